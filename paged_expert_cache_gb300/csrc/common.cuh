@@ -1,0 +1,219 @@
+// common.cuh -- device-side building blocks shared by the kernels of the
+// routed-MoE-over-LRU-expert-cache library (sm_103a).
+//
+// Slot layout. A slot holds one expert's three matrices (gate, up, down) in a
+// layout made for the m16n8k16 tensor-core fragment: a matrix of R rows and C
+// columns is cut into 16-row tiles (rt) and 64-column chunks (kc); the bytes
+// a lane needs for the four k16 steps of one (rt, kc) sit together, so one
+// 16-byte load per lane feeds four MMAs. Fragment coordinates for lane l:
+// g = l >> 2, q = l & 3; for k-step s the lane's A elements are
+//   a0 = (row g,   cols c0+2q, c0+2q+1)    a1 = (row g+8, same cols)
+//   a2 = (row g,   cols c0+2q+8, c0+2q+9)  a3 = (row g+8, same cols)
+// with c0 = kc*64 + s*16 and rows relative to rt*16. Byte counts per matrix
+// equal the canonical record's, so a slot is exactly a record's size.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum { FMT_BF16 = 0, FMT_Q4_0 = 1, FMT_FP8_B128 = 2, FMT_NVFP4 = 3 };
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 16;
+constexpr int kDecodeMaxTokens = 32;
+
+// Bytes of one matrix (R rows x C cols) in a slot; equals the canonical size.
+__host__ __device__ inline uint64_t matrix_bytes(int fmt, int R, int C) {
+    uint64_t r = (uint64_t)R, c = (uint64_t)C;
+    switch (fmt) {
+    case FMT_BF16: return r * c * 2;
+    case FMT_Q4_0: return r * (c / 32) * 18;
+    case FMT_FP8_B128: return r * c + ((r + 127) / 128) * ((c + 127) / 128) * 4;
+    case FMT_NVFP4: return r * c / 2 + r * (c / 16);
+    default: return 0;
+    }
+}
+
+// Bytes between matrices inside a slot: the matrix size rounded up to 16.
+__host__ __device__ inline uint64_t matrix_stride(int fmt, int R, int C) { return (matrix_bytes(fmt, R, C) + 15) & ~15ull; }
+
+// Per-call plan, written by the routing kernel and read by the others.
+struct Plan {
+    int n_uniq;   // distinct routed experts of the call
+    int n_hit;    // of those, resident at the start of the call
+    int n_fill;   // uploads into cache slots (decode) or arena stagings (prefill)
+    int n_units;  // compute units: n_uniq (+1 shared expert)
+    int status;   // 0 ok; 2 capacity exceeded (nothing changed)
+    int reranked; // 1 if the fp64 re-rank decided the top-k of some token
+    int pad[2];
+};
+
+// Device pointers of one call's scratch, passed by value to kernels.
+struct Scratch {
+    double* logits;     // [T][E]
+    double* bounds;     // [T][E] bound on distance from the defining fp64 sum
+    int* ids;           // [T*k] rank order per token
+    float* wts;         // [T*k]
+    int* slot_of;       // [T*k]
+    int* hit_of;        // [T*k]
+    int* unit_expert;   // [U]
+    int* unit_slot;     // [U] (-1: staged in the arena)
+    uint64_t* unit_src; // [U] device address of the unit's slot record
+    float* unit_g;      // [U*3] NVFP4 global scales (1 otherwise)
+    int* unit_pstart;   // [U+1] CSR offsets into unit_pairs
+    int* unit_pairs;    // [P]  pair ids: t*k + j, or T*k + t for the shared expert
+    int* pair_unit;     // [P]
+    uint64_t* copy_src; // [U] record copies: source (mapped host store)
+    uint64_t* copy_dst; // [U] record copies: destination (slot or arena)
+    int* copy_expert;   // [U] expert of each copy (the fill list)
+    int* copy_slot;     // [U] slot of each copy (-1 for arena stagings)
+    float* act;         // [P][I] SwiGLU activations
+    float* part;        // [P][H] down-projection partials per pair
+    Plan* plan;
+    unsigned* route_done;   // CTA counter of the routing kernel
+    unsigned* tile_done;    // [H/16] CTA counters of the down kernel
+    unsigned* copy_done;    // CTA counter of the copy kernel
+    unsigned long long* copy_t0;  // copy kernel start / end (globaltimer ns)
+    unsigned long long* copy_t1;
+};
+
+// Device cache state and constants of a handle.
+struct CacheDev {
+    int L, E, k, H, I, fmt, has_shared, n_pools, K, norm_topk;
+    int pool_mode;               // 0 per layer, 1 shared
+    uint64_t slot_stride, slot_bytes;
+    uint8_t* pool;               // [n_pools*K*stride]
+    const uint8_t* store;        // mapped pinned store [L*E*stride] (device alias)
+    const uint8_t* shared_w;     // [L*stride] or null
+    uint8_t* arena;              // [2*group*stride] or null
+    const float* gtable;         // [(L*E + L)*3] NVFP4 global scales
+    int* slot_map;               // [L*E]
+    int* key_of;                 // [n_pools*K]
+    unsigned long long* last_use;  // [n_pools*K] clock of the last use
+    unsigned long long* clock;     // [n_pools]
+    unsigned long long* stats;     // [3][5] + [15] re-rank count
+    int* trace;                    // ring of records, or null
+    unsigned long long* trace_count;
+    int trace_cap, trace_stride;
+};
+
+// ---------------------------------------------------------------------------
+// Tensor-core helpers (mma.sync m16n8k16, fp32 accumulate).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            const void* smem_row) {
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(smem_row);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a));
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+    return d;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Q4_0 word -> four fp16x2 A registers holding (q - 8) exactly. Nibble pairs
+// (bits 0-3|16-19) -> a0, (4-7|20-23) -> a1, (8-11|24-27) -> a2,
+// (12-15|28-31) -> a3. OR-ing a nibble into the mantissa of 1024.0 gives
+// 1024 + q (low position) or 1024 + 16 q (high position), both exact.
+__device__ __forceinline__ void q4_to_frag(uint32_t w, uint32_t a[4]) {
+    const uint32_t kMagic = 0x64006400u;  // 1024.0 in both halves
+    const __half2 k1032 = u32_as_h2(0x64086408u);   // 1032.0
+    const __half2 kSixteenth = u32_as_h2(0x2C002C00u);  // 1/16
+    const __half2 kM72 = u32_as_h2(0xD480D480u);    // -72.0
+    uint32_t t0 = lop3_and_or(w, 0x000f000fu, kMagic);
+    uint32_t t1 = lop3_and_or(w, 0x00f000f0u, kMagic);
+    uint32_t w8 = w >> 8;
+    uint32_t t2 = lop3_and_or(w8, 0x000f000fu, kMagic);
+    uint32_t t3 = lop3_and_or(w8, 0x00f000f0u, kMagic);
+    a[0] = h2_as_u32(__hsub2(u32_as_h2(t0), k1032));
+    a[1] = h2_as_u32(__hfma2(u32_as_h2(t1), kSixteenth, kM72));
+    a[2] = h2_as_u32(__hsub2(u32_as_h2(t2), k1032));
+    a[3] = h2_as_u32(__hfma2(u32_as_h2(t3), kSixteenth, kM72));
+}
+
+// Two e4m3 codes (low byte = lower column) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+    __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+
+// Two e2m1 codes in one byte (low nibble = lower column) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+    __half2_raw r = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(byte & 0xffu), __NV_E2M1);
+    return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+
+// ---------------------------------------------------------------------------
+// Kernel entry points (launch helpers defined in the .cu files).
+// ---------------------------------------------------------------------------
+struct RouteArgs {
+    const uint16_t* x;   // [T][H] bf16
+    const uint16_t* w;   // [E][H] bf16
+    const float* bias;   // [E] or null
+    int T, layer, prefill, bucket;
+};
+
+void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st);
+void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
+void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st);
+void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st);
+void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
+                   int units, cudaStream_t st);
+void launch_down(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,
+                 cudaStream_t st);
+size_t route_smem_bytes(const CacheDev& c, int T);
+
+// Host-side repack of canonical records into the slot layout (repack.cpp).
+void repack_record(int fmt, int H, int I, const uint8_t* canonical, uint8_t* slot, float* gscales3);
+
+}  // namespace moe

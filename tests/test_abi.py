@@ -1,0 +1,44 @@
+"""The C-ABI library loads, exports every entry point its header declares, and
+validates configurations on the host (no GPU needed)."""
+import ctypes
+
+import pytest
+
+import paged_expert_cache_gb300 as pec
+
+
+def test_library_exports_every_header_function():
+    lib = pec.load()
+    names = pec.header_functions()
+    assert "moe_layer_forward" in names and "moe_cache_create" in names and "moe_cache_stats" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.moe_abi_version() == 1
+
+
+def test_config_defaults():
+    c = pec.MoeConfig()
+    pec.load().moe_config_default(ctypes.byref(c))
+    assert c.norm_topk == 1 and c.max_cache_tokens == 32 and c.prefill_group == 32 and c.max_tokens == 32
+    assert c.upload_mode == 0 and c.pool_mode == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(L=0, E=16, k=2, H=256, I=128), pec.ERR_INVALID),
+    (dict(L=1, E=2000, k=2, H=256, I=128), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=17, H=256, I=128), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=100, I=128), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=96), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, fmt=7), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=4, H=256, I=128, slots_per_layer=3), pec.ERR_CAPACITY),
+    (dict(L=1, E=16, k=2, H=256, I=128, pool_mode="shared", pool_bytes=196608 * 2 - 1), pec.ERR_CAPACITY),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, max_cache_tokens=33), pec.ERR_INVALID),
+])
+def test_invalid_configurations_are_refused(kw, status):
+    args = dict(kw)
+    L, E, k, H, I = (args.pop(x) for x in ("L", "E", "k", "H", "I"))
+    cfg = pec.make_config(L, E, k, H, I, **args)
+    with pytest.raises(pec.MoeError) as ei:
+        pec.MoECache(cfg)
+    assert ei.value.status == status
+    assert str(ei.value)

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Routing (top-k ids in rank order), slot assignments, hit flags and fills are
+compared bit for bit on every call; layer outputs (fp32) must be within
+relative L2 1e-3 of the oracle's fp64 unpaged layer on every call.
+"""
+import numpy as np
+import pytest
+
+from harness import OracleRun, Setup, compare_trace, cuda_available, rel_l2
+from synth.workloads import WORKLOADS, scaled
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+TOL = 1e-3
+
+
+def run_steps(st, orc, steps, T, layers=None, check_out=True, out_every=1):
+    w = st.w
+    layers = range(w.L) if layers is None else layers
+    xs = {l: st.hiddens(l, T, steps) for l in layers}
+    worst = 0.0
+    for step in range(steps):
+        for l in layers:
+            x = xs[l][step]
+            y = st.forward(x, l)
+            ids, _ = orc.route(x, st.router[l], st.bias)
+            plan = orc.plan(l, ids, T)
+            recs = st.cache.trace_read()
+            assert len(recs) == 1
+            compare_trace(recs[0], ids, plan, l, T)
+            if check_out and step % out_every == 0:
+                _, _, yo = orc.layer(x, st.router[l], st.bias, l)
+                err = rel_l2(y, yo)
+                worst = max(worst, err)
+                assert err <= TOL, (step, l, err)
+    return worst
+
+
+def test_tiny_workload_full():
+    w = WORKLOADS["tiny"]
+    st = Setup(w)
+    orc = OracleRun(w, st.info["slot_bytes"])
+    worst = run_steps(st, orc, w.steps, w.streams[0])
+    g = st.cache.state()
+    o = orc.cache.state()
+    assert np.array_equal(g["slot_map"], o["slot_map"])
+    assert np.array_equal(g["key_of"], o["key_of"])
+    assert np.array_equal(g["order"], o["order"])
+    gs, os_ = st.cache.stats(), orc.cache.stats()
+    for b in range(3):
+        for key, okey in (("calls", "calls"), ("hits", "hits"), ("misses", "misses"), ("bytes_uploaded", "bytes")):
+            assert gs["buckets"][b][key] == os_[b][okey], (b, key)
+    print("tiny worst rel-L2", worst)
+    st.close()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q4_0", "fp8_b128", "nvfp4"])
+@pytest.mark.parametrize("pool_mode", ["per_layer", "shared"])
+def test_formats_small(fmt, pool_mode):
+    base = WORKLOADS["flash_next_nvfp4"]
+    # 3 layers, 40 experts top-4, H 512, I 192 (3 row chunks of 64 + ragged
+    # tile counts), tight pools so evictions happen every step
+    w = scaled(base, name="small", L=3, E=40, k=4, H=512, I=192, fmt=fmt, pool_mode=pool_mode,
+               slots_per_layer=10, pool_bytes=0.0, has_shared=(fmt in ("nvfp4", "q4_0")), bias=True,
+               streams=(3,), steps=10, rho=0.7)
+    from harness import pool_slots  # noqa
+    import oracle
+    sb = oracle.slot_bytes(fmt, w.H, w.I)
+    if pool_mode == "shared":
+        w = scaled(w, pool_bytes=sb * 16 + 5)
+    st = Setup(w)
+    assert st.info["slot_bytes"] == sb
+    orc = OracleRun(w, st.info["slot_bytes"])
+    worst = run_steps(st, orc, w.steps, 3)
+    g, o = st.cache.state(), orc.cache.state()
+    assert np.array_equal(g["order"], o["order"]) and np.array_equal(g["slot_map"], o["slot_map"])
+    print(fmt, pool_mode, "worst rel-L2", worst)
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 17, 32])
+def test_token_counts(T):
+    w = scaled(WORKLOADS["qwen3_30b_a3b_q4_0"], name="tok", L=2, E=64, k=8, H=256, I=128,
+               slots_per_layer=max(8 * T, 20), steps=3, streams=(T,))
+    st = Setup(w, max_tokens=32)
+    orc = OracleRun(w, st.info["slot_bytes"])
+    run_steps(st, orc, 3, T)
+    st.close()
+
+
+def test_paging_invariance_across_pool_sizes():
+    # The same calls with every expert resident, with the configured pool and
+    # with the smallest legal pool give bitwise identical outputs.
+    w = scaled(WORKLOADS["qwen3_30b_a3b_fp8"], name="inv", L=2, E=24, k=4, H=256, I=128, streams=(2,), steps=8)
+    outs = []
+    for K in (24, 12, 8):
+        st = Setup(w, K=K, trace=0)
+        xs = {l: st.hiddens(l, 2, w.steps) for l in range(w.L)}
+        ys = [st.forward(xs[l][s], l) for s in range(w.steps) for l in range(w.L)]
+        outs.append(np.stack(ys))
+        st.close()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_upload_modes_agree_and_slots_hold_the_store_bytes():
+    w = scaled(WORKLOADS["qwen3_30b_a3b_q4_0"], name="upl", L=2, E=24, k=4, H=256, I=128, streams=(2,), steps=6,
+               slots_per_layer=9)
+    res = {}
+    for mode in ("pull", "memcpy"):
+        st = Setup(w, upload=mode)
+        orc = OracleRun(w, st.info["slot_bytes"])
+        xs = {l: st.hiddens(l, 2, w.steps) for l in range(w.L)}
+        ys = []
+        for s in range(w.steps):
+            for l in range(w.L):
+                ys.append(st.forward(xs[l][s], l))
+                ids, _ = orc.route(xs[l][s], st.router[l], st.bias)
+                plan = orc.plan(l, ids, 2)
+                rec = st.cache.trace_read()[0]
+                compare_trace(rec, ids, plan, l, 2)
+        res[mode] = np.stack(ys)
+        # every occupied slot holds its expert's store bytes exactly
+        state = st.cache.state()
+        for p in range(state["key_of"].shape[0]):
+            for s, key in enumerate(state["key_of"][p]):
+                if key < 0:
+                    continue
+                dev_bytes, store_bytes = st.cache.read_slot(p, s, key // w.E, key % w.E)
+                assert np.array_equal(dev_bytes, store_bytes), (mode, p, s, key)
+        stats = st.cache.stats()
+        assert stats["buckets"][0]["misses"] > 0 and stats["buckets"][0]["upload_ns"] > 0
+        st.close()
+    assert np.array_equal(res["pull"], res["memcpy"])
+
+
+def test_prefill_path_reads_in_place_and_keeps_the_lru():
+    w = scaled(WORKLOADS["flash_next_prefill"], name="pre", L=2, E=48, k=4, H=256, I=128, pool_mode="shared",
+               pool_bytes=0.0, streams=(2,), steps=4, prompt_T=80)
+    import oracle
+    import synth
+    sb = oracle.slot_bytes(w.fmt, w.H, w.I)
+    w = scaled(w, pool_bytes=sb * 20)
+    st = Setup(w, max_tokens=80)
+    orc = OracleRun(w, st.info["slot_bytes"])
+    # warm the cache with a few decode calls
+    run_steps(st, orc, 3, 2, check_out=False)
+    before = st.cache.state()
+    for l in range(w.L):
+        x = synth.prompt(w.seed, l, 80, w.H)
+        y = st.forward(x, l)
+        ids, _ = orc.route(x, st.router[l], st.bias)
+        plan = orc.plan(l, ids, 80)
+        rec = st.cache.trace_read()[0]
+        assert np.array_equal(rec["ids"], ids.reshape(-1))
+        assert np.array_equal(rec["hit_of"].astype(np.uint8), plan["hit_of"])
+        assert np.array_equal(rec["slot_of"], plan["slot_of"])
+        _, _, yo = orc.layer(x, st.router[l], st.bias, l)
+        assert rel_l2(y, yo) <= TOL
+    after = st.cache.state()
+    for key in before:
+        assert np.array_equal(before[key], after[key])
+    s = st.cache.stats()["buckets"][2]
+    o = orc.cache.stats()[2]
+    assert s["calls"] == o["calls"] == 2 and s["hits"] == o["hits"] and s["misses"] == o["misses"]
+    st.close()
+
+
+def test_capacity_rule_refuses_without_changing_state():
+    import paged_expert_cache_gb300 as pec
+    w = scaled(WORKLOADS["tiny"], name="cap", steps=2, streams=(4,))
+    st = Setup(w)
+    x = st.hiddens(0, 4, 1)[0]
+    st.forward(x, 0)
+    before = st.cache.state()
+    x5 = st.hiddens(0, 5, 1)[0]  # 5 tokens * top-2 = 10 > 8 slots
+    with pytest.raises(pec.MoeError) as ei:
+        st.forward(x5, 0)
+    assert ei.value.status == pec.ERR_CAPACITY
+    after = st.cache.state()
+    for key in before:
+        assert np.array_equal(before[key], after[key])
+    st.close()
+
+
+def test_exact_ties_rank_the_lower_expert_first():
+    import torch
+    w = scaled(WORKLOADS["tiny"], name="ties", E=16, k=4, steps=4, streams=(3,), bias=False)
+    st = Setup(w)
+    # duplicate router rows: experts (3, 9) and (5, 12) tie on every input
+    r = st.router[0].copy()
+    r[9] = r[3]
+    r[12] = r[5]
+    st.router[0] = r
+    st.router_dev[0] = torch.from_numpy(r.view(np.int16)).to(st.dev)
+    orc = OracleRun(w, st.info["slot_bytes"])
+    run_steps(st, orc, 4, 3)
+    assert st.cache.stats()["topk_fp64_rerank"] > 0
+    st.close()
