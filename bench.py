@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Decode benchmark of the routed MoE FFN over the LRU expert cache.
+
+Workload (default): Qwen3-30B-A3B-shaped decode -- 48 MoE layers, 128 experts
+per layer, top-8, hidden 2048, expert intermediate 768, Q4_0 experts, 92 LRU
+slots per layer, batch 1, AR(1) hiddens (rho 0.9). One step is one decode
+token through all 48 layers: router + top-k, the cache plan, miss uploads
+from the pinned host store, gate/up + SwiGLU and down + combine, all through
+moe_layer_forward. Inputs are seeded synthetic stand-ins for the pages'
+checkpoints and prompts.
+
+Prints ONE JSON line (rank 0). --impl reference times the CPU oracle instead.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode tok/s (batch 1–32) + expert-FFN HBM GB/s vs ~8 TB/s peak; hit rate"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_30b_a3b_q4_0")
+    ap.add_argument("--batch", type=int, default=0, help="tokens per call (default: the workload's first)")
+    ap.add_argument("--profile-steps", type=int, default=32)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU sample")
+    ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
+    return ap.parse_args()
+
+
+def matrix_bytes(fmt, R, C):
+    """Bytes of one weight matrix in a record (layouts of include/moe_cache.h)."""
+    if fmt == "bf16":
+        return R * C * 2
+    if fmt == "q4_0":
+        return R * (C // 32) * 18
+    if fmt == "fp8_b128":
+        return R * C + ((R + 127) // 128) * ((C + 127) // 128) * 4
+    return R * C // 2 + R * (C // 16)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs", 6800.0), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling through NVML (read-only queries)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, torch_dev):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(torch_dev)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch_dev), ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            m = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _loop(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value & ~0x1
+            time.sleep(0.002)
+
+    def start(self):
+        if not self.ok:
+            return
+        self._stop = threading.Event()
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        self._stop.set()
+        self._t.join()
+        names = [n for b, n in self.REASONS.items() if self.reasons & b]
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def cpu_sample(w, T, budget_s, layers_per_step=None):
+    """Runs the oracle (routing, literal LRU, unpaged layer) token by token
+    through the workload's layers until budget_s is spent; returns tok/s."""
+    import numpy as np
+    import oracle
+    import synth
+    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer if w.pool_mode == "per_layer" else
+                         oracle.slots_for_budget(w.pool_bytes, oracle.slot_bytes(w.fmt, w.H, w.I)),
+                         oracle.slot_bytes(w.fmt, w.H, w.I))
+    bias = synth.zipf_bias(w.E) if w.bias else None
+    routers = {}
+    recs = {}
+    layer_s = 0.0
+    layers_done = 0
+    steps = max(2, int(budget_s))
+    xs = {}
+    t_start = time.perf_counter()
+    for step in range(steps):
+        for l in range(w.L if layers_per_step is None else layers_per_step):
+            if l not in routers:
+                routers[l] = synth.router_weights(w.seed, l, w.E, w.H)
+                xs[l] = np.stack([synth.hidden_ar1(w.seed, l, s, steps, w.H, w.rho) for s in range(T)], axis=1)
+            x = xs[l][step]
+            z = oracle.router_logits(x, routers[l], bias)
+            ids, _ = oracle.topk(z, w.k)
+            need = {int(e) for e in np.unique(ids)}
+            for e in need:  # record generation is input preparation, outside the timing
+                if (l, e) not in recs:
+                    recs[(l, e)] = synth.expert_record(w.fmt, w.seed, l, e, w.H, w.I)
+            shared = None
+            if w.has_shared:
+                if (l, -1) not in recs:
+                    recs[(l, -1)] = synth.expert_record(w.fmt, w.seed, l, -1, w.H, w.I)
+                shared = recs[(l, -1)]
+            t0 = time.perf_counter()
+            z = oracle.router_logits(x, routers[l], bias)
+            ids, _ = oracle.topk(z, w.k)
+            cache.plan(l, ids.reshape(-1), T)
+            oracle.moe_layer(w.fmt, w.H, w.I, w.E, w.k, {e: recs[(l, e)] for e in need}, x, routers[l], bias,
+                             shared=shared)
+            layer_s += time.perf_counter() - t0
+            layers_done += 1
+            if layer_s >= budget_s or time.perf_counter() - t_start > 4 * budget_s:
+                break
+        if layer_s >= budget_s or time.perf_counter() - t_start > 4 * budget_s:
+            break
+    tokens = layers_done * T / w.L
+    return tokens / layer_s, layers_done, layer_s
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synth.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    T = args.batch or w.streams[0]
+    # a step is one layer call of T tokens (a bounded sample of a decode token)
+    import numpy as np
+    import oracle
+    import synth
+    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer, oracle.slot_bytes(w.fmt, w.H, w.I))
+    bias = synth.zipf_bias(w.E) if w.bias else None
+    total = args.warmup + args.steps
+    routers, xs, recs = {}, {}, {}
+    elapsed = 0.0
+    for i in range(total):
+        l = i % w.L
+        step = i // w.L
+        if l not in routers:
+            routers[l] = synth.router_weights(w.seed, l, w.E, w.H)
+            xs[l] = np.stack([synth.hidden_ar1(w.seed, l, s, total // w.L + 1, w.H, w.rho) for s in range(T)], axis=1)
+        x = xs[l][step]
+        ids, _ = oracle.topk(oracle.router_logits(x, routers[l], bias), w.k)
+        for e in np.unique(ids):
+            if (l, int(e)) not in recs:
+                recs[(l, int(e))] = synth.expert_record(w.fmt, w.seed, l, int(e), w.H, w.I)
+        t0 = time.perf_counter()
+        ids, _ = oracle.topk(oracle.router_logits(x, routers[l], bias), w.k)
+        cache.plan(l, ids.reshape(-1), T)
+        oracle.moe_layer(w.fmt, w.H, w.I, w.E, w.k, {int(e): recs[(l, int(e))] for e in np.unique(ids)}, x,
+                         routers[l], bias)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            elapsed += dt
+    tokens = args.steps * T / w.L
+    v = tokens / elapsed
+    sample = f"{args.steps} layer calls of {T} token(s) (one layer of {w.L} per step), oracle fp64, 1 thread"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k,
+                       "format": w.fmt, "slots_per_layer": w.slots_per_layer},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import synth
+    from paged_expert_cache_gb300 import build as cbuild
+    synth.build()
+    cbuild.build()
+    import paged_expert_cache_gb300 as pec
+    from synth.workloads import WORKLOADS, scaled
+    w = WORKLOADS[args.workload]
+    T = args.batch or w.streams[0]
+    if rank:  # independent replicas: each rank draws its own inputs
+        w = scaled(w, index=w.index + 100 * rank)
+    if args.layers:
+        w = scaled(w, L=args.layers)
+    dev = torch.device("cuda", local)
+    cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
+                          slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
+                          max_tokens=max(T, 1), device=local)
+    t_setup = time.perf_counter()
+    cache = pec.MoECache(cfg)
+    buf = None
+    for l in range(w.L):
+        buf = synth.expert_records(w.fmt, w.seed, l, 0, w.E, w.H, w.I, out=buf)
+        cache.load_experts(l, 0, buf)
+        if w.has_shared:
+            cache.load_shared(l, synth.expert_record(w.fmt, w.seed, l, -1, w.H, w.I))
+    info = cache.info()
+    routers = torch.stack([torch.from_numpy(synth.router_weights(w.seed, l, w.E, w.H).view(np.int16))
+                           for l in range(w.L)]).to(dev)
+    bias = torch.from_numpy(synth.zipf_bias(w.E)).to(dev) if w.bias else None
+    n_total = args.warmup + 2 * args.steps + args.profile_steps
+    hid = np.empty((n_total, w.L, T, w.H), dtype=np.uint16)
+    for l in range(w.L):
+        for s in range(T):
+            hid[:, l, s, :] = synth.hidden_ar1(w.seed, l, s, n_total, w.H, w.rho)
+    hid_dev = torch.from_numpy(hid.view(np.int16)).to(dev)  # every input resident in HBM before timing
+    x_cur = torch.empty((w.L, T, w.H), dtype=torch.int16, device=dev)
+    out = torch.empty((w.L, T, w.H), dtype=torch.float32, device=dev)
+    setup_s = time.perf_counter() - t_setup
+
+    def step_layers():
+        for l in range(w.L):
+            cache.forward(x_cur[l], routers[l], l, out[l], bias=bias, T=T)
+
+    cursor = 0
+
+    def next_inputs():
+        nonlocal cursor
+        x_cur.copy_(hid_dev[cursor])
+        cursor += 1
+
+    # warm-up (eager; also sets every kernel attribute before capture)
+    for _ in range(args.warmup):
+        next_inputs()
+        step_layers()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(graph, stream=cap_stream):
+                step_layers()
+        torch.cuda.synchronize()
+
+    def run_step():
+        next_inputs()
+        if graph is not None:
+            graph.replay()
+        else:
+            step_layers()
+
+    s0 = cache.stats()
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        run_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    s1 = cache.stats()
+    b0, b1 = s0["buckets"][0], s1["buckets"][0]
+    hits, misses = b1["hits"] - b0["hits"], b1["misses"] - b0["misses"]
+    up_bytes = b1["bytes_uploaded"] - b0["bytes_uploaded"]
+    up_ns = b1["upload_ns"] - b0["upload_ns"]
+    tokens = args.steps * T * world
+    value = tokens / (ms / 1e3)
+
+    # e2e: inputs from pinned host memory each step, outputs read back each step
+    h_in = torch.from_numpy(hid[args.warmup + args.steps:args.warmup + 2 * args.steps].view(np.int16)).pin_memory()
+    h_out = torch.empty((w.L, T, w.H), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        x_cur.copy_(h_in[i], non_blocking=True)
+        if graph is not None:
+            graph.replay()
+        else:
+            step_layers()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    cursor = args.warmup + 2 * args.steps
+
+    # per-stage device time on a profiled pass over further steps (eager)
+    cache.profile_read()
+    cache.profile_enable(True)
+    sp0 = cache.stats()
+    for _ in range(args.profile_steps):
+        next_inputs()
+        step_layers()
+    prof = cache.profile_read()
+    cache.profile_enable(False)
+    sp1 = cache.stats()
+    peaks = load_peaks()
+    mgu = matrix_bytes(w.fmt, w.I, w.H)
+    mdn = matrix_bytes(w.fmt, w.H, w.I)
+    units = min(T * w.k, w.E)  # distinct experts per call at batch 1 (top_k picks are distinct)
+    gu_bytes = units * 2 * mgu + T * w.H * 2 + units * T * w.I * 4
+    dn_bytes = units * mdn + units * T * w.I * 4 + T * w.H * 4
+    stage_total = sum(v["ms"] for v in prof.values())
+    per = {k: (v["ms"] / v["launches"] if v["launches"] else 0.0) for k, v in prof.items()}
+    share = {k: (v["ms"] / stage_total if stage_total else 0.0) for k, v in prof.items()}
+    gu_gbs = gu_bytes / (per["gateup"] * 1e-3) / 1e9 if per["gateup"] else 0.0
+    dn_gbs = dn_bytes / (per["down"] * 1e-3) / 1e9 if per["down"] else 0.0
+    ffn_ms = prof["route"]["ms"] + prof["gateup"]["ms"] + prof["down"]["ms"]
+    ffn_bytes_step = w.L * (units * (2 * mgu + mdn) + w.E * w.H * 2)
+    ffn_gbs = ffn_bytes_step * args.profile_steps / (ffn_ms * 1e-3) / 1e9 if ffn_ms else 0.0
+    pmiss = sp1["buckets"][0]["misses"] - sp0["buckets"][0]["misses"]
+    dominant = max(("gateup", "down", "route", "copy"), key=lambda k: prof[k]["ms"])
+
+    # traffic from the committed ncu summary of the current kernels, if any
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            tj = json.load(open(tfile))
+            if tj.get("workload") == w.name and tj.get("kernel") == "gateup":
+                traffic = tj.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = {"bound": "hbm", "kernel": "k_gateup (gate/up + SwiGLU GEMV)", "achieved": gu_gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / peaks["hbm_gbs"],
+                "peak_src": peaks["src"], "traffic": traffic, "algorithmic_bytes_per_launch": gu_bytes,
+                "avg_launch_us": per["gateup"] * 1e3, "dominant_stage": dominant}
+
+    cpu = None
+    if rank == 0 and args.cpu_seconds > 0:
+        v, layers, secs = cpu_sample(w, T, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"{layers} layer calls ({layers / w.L:.2f} tokens) of the same workload, "
+                         f"{secs:.1f} s of fp64 oracle time on 1 host thread"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "q4_0 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
+                   "inter": w.I, "format": w.fmt, "slots_per_layer": w.slots_per_layer,
+                   "pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
+                   "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
+                   "l2": "inputs larger than L2: each step reads ~1 GB of distinct expert bytes from an "
+                         f"{info['pool_device_bytes'] / 1e9:.1f} GB slot pool"},
+        "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
+        "upload_gbs": up_bytes / up_ns if up_ns else None,
+        "expert_ffn_gbs": ffn_gbs, "expert_ffn_frac_of_8tbs": ffn_gbs / 8000.0,
+        "kernel_gbs": {"gateup": gu_gbs, "down": dn_gbs},
+        "stage_us_per_launch": {k: per[k] * 1e3 for k in ("route", "copy", "gateup", "down")},
+        "stage_share": {k: share[k] for k in ("route", "copy", "gateup", "down")},
+        "profiled_steps": args.profile_steps, "profiled_misses": pmiss,
+        "roofline": roofline,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tok/s",
+                "h2d_bytes_per_step": w.L * T * w.H * 2, "d2h_bytes_per_step": w.L * T * w.H * 4},
+        "gpu_launches": args.steps * w.L * 4 * world,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "setup_s": setup_s,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    cache.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -219,6 +219,22 @@ moe_status_t moe_cache_get_state(moe_cache_t* h, int32_t* slot_map, int32_t* key
 moe_status_t moe_cache_read_slot(moe_cache_t* h, int32_t pool, int32_t slot, void* dst,
                                  int32_t layer, int32_t expert, void* store_dst, uint64_t bytes);
 
+/* Per-stage device timing for measurement: when enabled, every kernel a
+ * forward launches is bracketed by CUDA events on the forward's stream (do
+ * not enable it while capturing a CUDA graph). Stages: 0 router + top-k +
+ * plan, 1 miss copies, 2 gate/up + SwiGLU, 3 down + combine, 4 prefill top-k,
+ * 5 prefill plan. */
+#define MOE_NUM_STAGES 6
+typedef struct {
+    double ms[MOE_NUM_STAGES];         /* summed event time per stage */
+    uint64_t launches[MOE_NUM_STAGES]; /* kernels timed per stage */
+} moe_profile_t;
+
+moe_status_t moe_cache_profile_enable(moe_cache_t* h, int32_t on);
+
+/* Synchronises, returns the totals since the last read and clears them. */
+moe_status_t moe_cache_profile_read(moe_cache_t* h, moe_profile_t* out);
+
 /* Synchronises, empties every slot, restores the initial LRU order and clears
  * the counters and trace. Expert data stays loaded. */
 moe_status_t moe_cache_reset(moe_cache_t* h);

@@ -48,6 +48,14 @@ class MoeInfo(ctypes.Structure):
                 ("scratch_device_bytes", u64)]
 
 
+NUM_STAGES = 6
+STAGES = ["route", "copy", "gateup", "down", "prefill_topk", "prefill_plan"]
+
+
+class MoeProfile(ctypes.Structure):
+    _fields_ = [("ms", dbl * NUM_STAGES), ("launches", u64 * NUM_STAGES)]
+
+
 _lib = None
 
 
@@ -78,6 +86,8 @@ def load():
         "moe_cache_trace_read": (i32, [vp, vp, ctypes.c_int64, P(ctypes.c_int64), P(i32)]),
         "moe_cache_get_state": (i32, [vp, vp, vp, vp]),
         "moe_cache_read_slot": (i32, [vp, i32, i32, vp, i32, i32, vp, u64]),
+        "moe_cache_profile_enable": (i32, [vp, i32]),
+        "moe_cache_profile_read": (i32, [vp, P(MoeProfile)]),
         "moe_cache_reset": (i32, [vp]),
         "moe_cache_destroy": (i32, [vp]),
     }
@@ -247,6 +257,14 @@ class MoECache:
         _check(load().moe_cache_read_slot(self.h, pool, slot, dst.ctypes.data, layer, expert,
                                           None if store is None else store.ctypes.data, nbytes), self.h)
         return dst, store
+
+    def profile_enable(self, on=True):
+        _check(load().moe_cache_profile_enable(self.h, 1 if on else 0), self.h)
+
+    def profile_read(self):
+        p = MoeProfile()
+        _check(load().moe_cache_profile_read(self.h, ctypes.byref(p)), self.h)
+        return {STAGES[i]: {"ms": p.ms[i], "launches": p.launches[i]} for i in range(NUM_STAGES)}
 
     def reset(self):
         _check(load().moe_cache_reset(self.h), self.h)

@@ -33,6 +33,12 @@ struct moe_cache {
     uint64_t memcpy_upload_ns[3] = {0, 0, 0};
     int trace_cap = 0, trace_stride = 0;
     std::vector<float> gtable_host;
+    // per-stage event timing
+    bool prof_on = false;
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+    struct Span { int stage, a, b; };
+    std::vector<Span> spans;
 };
 
 namespace {
@@ -64,7 +70,29 @@ cudaError_t dalloc(moe_cache_t* h, T** p, size_t n) {
     return e;
 }
 
+int prof_event(moe_cache_t* h, cudaStream_t st) {
+    if (h->ev_used == h->ev_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return -1;
+        h->ev_pool.push_back(e);
+    }
+    cudaEventRecord(h->ev_pool[h->ev_used], st);
+    return (int)h->ev_used++;
+}
+
+// Brackets one launch with events when profiling is on.
+template <typename F>
+void timed(moe_cache_t* h, int stage, cudaStream_t st, F&& launch) {
+    if (!h->prof_on) { launch(); return; }
+    int a = prof_event(h, st);
+    launch();
+    int b = prof_event(h, st);
+    if (a >= 0 && b >= 0) h->spans.push_back({stage, a, b});
+}
+
 void free_all(moe_cache_t* h) {
+    for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+    h->ev_pool.clear();
     for (void* p : h->dev_allocs) cudaFree(p);
     h->dev_allocs.clear();
     if (h->store_host) cudaFreeHost(h->store_host);
@@ -353,9 +381,9 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     a.bucket = bucket;
     const int units = std::min(T * d.k, d.E) + d.has_shared;
     if (decode) {
-        moe::launch_route(d, h->scr, a, units, st);
+        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st); });
         if (h->cfg.upload_mode == MOE_UPLOAD_PULL) {
-            moe::launch_copy(d, h->scr, 0, h->maxU, bucket, st);
+            timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, 0, h->maxU, bucket, st); });
         } else {
             // read the fill list back, then one copy per merged run
             int* hf = h->host_fill;
@@ -384,19 +412,19 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
                                                    .count();
             }
         }
-        moe::launch_gateup(d, h->scr, a.x, T, 0, 0, h->G, units, st);
-        moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, st);
+        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 0, 0, h->G, units, st); });
+        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, st); });
     } else {
-        moe::launch_route(d, h->scr, a, units, st);
-        moe::launch_topk_prefill(d, h->scr, a, st);
-        moe::launch_plan_prefill(d, h->scr, a, h->G, st);
-        moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st);
-        moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, st);
+        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st); });
+        timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });
+        timed(h, 5, st, [&] { moe::launch_plan_prefill(d, h->scr, a, h->G, st); });
+        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st); });
+        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, st); });
         const int groups = (std::min(T * d.k, d.E) + h->G - 1) / h->G;
         for (int g = 0; g < groups; ++g) {
-            moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st);
-            moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st);
-            moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, st);
+            timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
+            timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st); });
+            timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, st); });
         }
     }
     cudaError_t e = cudaGetLastError();
@@ -524,6 +552,28 @@ moe_status_t moe_cache_read_slot(moe_cache_t* h, int32_t pool, int32_t slot, voi
             return fail(h, MOE_ERR_INVALID, "bad layer or expert");
         memcpy(store_dst, h->store_host + ((size_t)layer * d.E + expert) * h->slot_stride, bytes);
     }
+    return MOE_OK;
+}
+
+moe_status_t moe_cache_profile_enable(moe_cache_t* h, int32_t on) {
+    if (!h) return fail(nullptr, MOE_ERR_INVALID, "handle is NULL");
+    h->prof_on = on != 0;
+    return MOE_OK;
+}
+
+moe_status_t moe_cache_profile_read(moe_cache_t* h, moe_profile_t* out) {
+    if (!h || !out) return fail(h, MOE_ERR_INVALID, "NULL argument");
+    memset(out, 0, sizeof(*out));
+    CK(h, cudaSetDevice(h->cfg.device));
+    CK(h, cudaDeviceSynchronize());
+    for (const auto& sp : h->spans) {
+        float ms = 0.f;
+        CK(h, cudaEventElapsedTime(&ms, h->ev_pool[sp.a], h->ev_pool[sp.b]));
+        out->ms[sp.stage] += ms;
+        out->launches[sp.stage] += 1;
+    }
+    h->spans.clear();
+    h->ev_used = 0;
     return MOE_OK;
 }
 

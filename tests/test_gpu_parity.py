@@ -62,7 +62,7 @@ def test_formats_small(fmt, pool_mode):
     # 3 layers, 40 experts top-4, H 512, I 192 (3 row chunks of 64 + ragged
     # tile counts), tight pools so evictions happen every step
     w = scaled(base, name="small", L=3, E=40, k=4, H=512, I=192, fmt=fmt, pool_mode=pool_mode,
-               slots_per_layer=10, pool_bytes=0.0, has_shared=(fmt in ("nvfp4", "q4_0")), bias=True,
+               slots_per_layer=14, pool_bytes=0.0, has_shared=(fmt in ("nvfp4", "q4_0")), bias=True,
                streams=(3,), steps=10, rho=0.7)
     from harness import pool_slots  # noqa
     import oracle
@@ -169,7 +169,7 @@ def test_prefill_path_reads_in_place_and_keeps_the_lru():
 def test_capacity_rule_refuses_without_changing_state():
     import paged_expert_cache_gb300 as pec
     w = scaled(WORKLOADS["tiny"], name="cap", steps=2, streams=(4,))
-    st = Setup(w)
+    st = Setup(w, max_tokens=8)
     x = st.hiddens(0, 4, 1)[0]
     st.forward(x, 0)
     before = st.cache.state()
@@ -185,7 +185,7 @@ def test_capacity_rule_refuses_without_changing_state():
 
 def test_exact_ties_rank_the_lower_expert_first():
     import torch
-    w = scaled(WORKLOADS["tiny"], name="ties", E=16, k=4, steps=4, streams=(3,), bias=False)
+    w = scaled(WORKLOADS["tiny"], name="ties", E=16, k=4, steps=4, streams=(3,), bias=False, slots_per_layer=12)
     st = Setup(w)
     # duplicate router rows: experts (3, 9) and (5, 12) tie on every input
     r = st.router[0].copy()
