@@ -92,8 +92,8 @@ typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_experts;      /* E routed experts per layer, 1..1024 */
     int32_t top_k;            /* k, 1..16 and <= E */
-    int32_t hidden;           /* H, multiple of 64 */
-    int32_t inter;            /* I, expert intermediate size, multiple of 64 */
+    int32_t hidden;           /* H, multiple of 64, at most 4096 */
+    int32_t inter;            /* I, expert intermediate size, multiple of 64, at most 4096 */
     int32_t format;           /* moe_format_t */
     int32_t has_shared;       /* 1: an always-resident shared expert per layer */
     int32_t pool_mode;        /* moe_pool_mode_t */

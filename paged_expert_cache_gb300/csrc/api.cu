@@ -156,6 +156,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         return fail(nullptr, MOE_ERR_INVALID, "top_k must be in 1..min(16, num_experts)");
     if (c.hidden < 64 || c.hidden % 64 || c.inter < 64 || c.inter % 64)
         return fail(nullptr, MOE_ERR_INVALID, "hidden and inter must be positive multiples of 64");
+    if (c.hidden > 4096 || c.inter > 4096) return fail(nullptr, MOE_ERR_INVALID, "hidden and inter must be <= 4096");
     if (!valid_fmt(c.format)) return fail(nullptr, MOE_ERR_INVALID, "unknown format");
     if (c.pool_mode != MOE_POOL_PER_LAYER && c.pool_mode != MOE_POOL_SHARED)
         return fail(nullptr, MOE_ERR_INVALID, "unknown pool_mode");
@@ -172,6 +173,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     d.L = c.num_layers; d.E = c.num_experts; d.k = c.top_k; d.H = c.hidden; d.I = c.inter;
     d.fmt = c.format; d.has_shared = c.has_shared ? 1 : 0; d.norm_topk = c.norm_topk ? 1 : 0;
     d.pool_mode = c.pool_mode;
+    d.fused_upload = c.upload_mode == MOE_UPLOAD_PULL ? 1 : 0;
     const uint64_t cgu = moe::matrix_bytes(d.fmt, d.I, d.H), cdn = moe::matrix_bytes(d.fmt, d.H, d.I);
     h->record_bytes = 2 * cgu + cdn + (d.fmt == moe::FMT_NVFP4 ? 12 : 0);
     h->slot_bytes = 2 * moe::matrix_stride(d.fmt, d.I, d.H) + moe::matrix_stride(d.fmt, d.H, d.I);
@@ -257,11 +259,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.wts, T * d.k);
     DA(s.slot_of, T * d.k);
     DA(s.hit_of, T * d.k);
-    DA(s.unit_expert, U);
-    DA(s.unit_slot, U);
-    DA(s.unit_src, U);
-    DA(s.unit_g, U * 3);
-    DA(s.unit_pstart, U + 1);
+    DA(s.units, U);
     DA(s.unit_pairs, P);
     DA(s.pair_unit, P);
     DA(s.copy_src, U);
@@ -276,11 +274,13 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.copy_done, 1);
     DA(s.copy_t0, 1);
     DA(s.copy_t1, 1);
+    DA(s.tiles_done, 1);
 #undef DA
-    h->scratch_bytes = T * d.E * 16 + T * d.k * 16 + U * 48 + P * 8 + P * (d.I + d.H) * 4;
+    h->scratch_bytes = T * d.E * 16 + T * d.k * 16 + U * (sizeof(moe::UnitDesc) + 32) + P * 8 + P * (d.I + d.H) * 4;
     if (cudaMemset(s.route_done, 0, 4) != cudaSuccess || cudaMemset(s.tile_done, 0, (d.H / 16) * 4) != cudaSuccess ||
         cudaMemset(s.copy_done, 0, 4) != cudaSuccess || cudaMemset(s.copy_t0, 0xff, 8) != cudaSuccess ||
-        cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess)
+        cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess ||
+        cudaMemset(s.tiles_done, 0, 4) != cudaSuccess)
         return bail(MOE_ERR_CUDA, "scratch initialisation failed");
     if (c.upload_mode == MOE_UPLOAD_MEMCPY) {
         e = cudaHostAlloc((void**)&h->host_fill, sizeof(int) * (2 + 2 * U), cudaHostAllocDefault);
@@ -380,11 +380,15 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     a.prefill = decode ? 0 : 1;
     a.bucket = bucket;
     const int units = std::min(T * d.k, d.E) + d.has_shared;
+    // programmatic dependent launch between the decode kernels (off while
+    // events bracket each launch for profiling)
+    const bool pdl = !h->prof_on;
     if (decode) {
-        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st); });
-        if (h->cfg.upload_mode == MOE_UPLOAD_PULL) {
-            timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, 0, h->maxU, bucket, st); });
-        } else {
+        // PULL: misses are pulled over the host link by the expert kernels
+        // themselves (gate/up and down each stream their part of a missed
+        // record into its slot while they consume it)
+        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, pdl); });
+        if (h->cfg.upload_mode == MOE_UPLOAD_MEMCPY) {
             // read the fill list back, then one copy per merged run
             int* hf = h->host_fill;
             CK(h, cudaMemcpyAsync(hf, &h->scr.plan->n_fill, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -412,19 +416,19 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
                                                    .count();
             }
         }
-        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 0, 0, h->G, units, st); });
-        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, st); });
+        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 0, 0, h->G, units, st, pdl); });
+        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, bucket, st, pdl); });
     } else {
-        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st); });
+        timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, false); });
         timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });
         timed(h, 5, st, [&] { moe::launch_plan_prefill(d, h->scr, a, h->G, st); });
-        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st); });
-        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, st); });
+        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st, false); });
+        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, bucket, st, false); });
         const int groups = (std::min(T * d.k, d.E) + h->G - 1) / h->G;
         for (int g = 0; g < groups; ++g) {
             timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
-            timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st); });
-            timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, st); });
+            timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st, false); });
+            timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, bucket, st, false); });
         }
     }
     cudaError_t e = cudaGetLastError();

@@ -54,19 +54,31 @@ struct Plan {
     int pad[2];
 };
 
+// One compute unit of a call (a distinct routed expert, or the shared
+// expert): where its weights are read from, where a missed expert's bytes
+// are written while they are read (0 for none), and its token pairs.
+struct UnitDesc {
+    uint64_t src;   // device address of the record the weights are read from
+    uint64_t dst;   // slot the record is written into on the way (a miss), or 0
+    float g[3];     // NVFP4 global scales of gate, up, down (1 otherwise)
+    int pstart;     // first entry in unit_pairs
+    int np;         // number of pairs
+    int expert;     // routed expert id, -1 for the shared expert
+    int slot;       // cache slot, -1 when staged or shared
+    int hit;        // resident at the start of the call
+    int pair8[8];   // the first eight entries of the unit's pair list
+};
+static_assert(sizeof(UnitDesc) == 80, "UnitDesc layout");
+
 // Device pointers of one call's scratch, passed by value to kernels.
 struct Scratch {
-    double* logits;     // [T][E]
-    double* bounds;     // [T][E] bound on distance from the defining fp64 sum
+    UnitDesc* units;    // [U]
+    float2* logits;     // [T][E] normalized float pair (hi, lo): hi = RN(hi + lo)
+    float* bounds;      // [T][E] bound on the pair's distance from the defining fp64 sum
     int* ids;           // [T*k] rank order per token
     float* wts;         // [T*k]
     int* slot_of;       // [T*k]
     int* hit_of;        // [T*k]
-    int* unit_expert;   // [U]
-    int* unit_slot;     // [U] (-1: staged in the arena)
-    uint64_t* unit_src; // [U] device address of the unit's slot record
-    float* unit_g;      // [U*3] NVFP4 global scales (1 otherwise)
-    int* unit_pstart;   // [U+1] CSR offsets into unit_pairs
     int* unit_pairs;    // [P]  pair ids: t*k + j, or T*k + t for the shared expert
     int* pair_unit;     // [P]
     uint64_t* copy_src; // [U] record copies: source (mapped host store)
@@ -79,14 +91,16 @@ struct Scratch {
     unsigned* route_done;   // CTA counter of the routing kernel
     unsigned* tile_done;    // [H/16] CTA counters of the down kernel
     unsigned* copy_done;    // CTA counter of the copy kernel
-    unsigned long long* copy_t0;  // copy kernel start / end (globaltimer ns)
+    unsigned long long* copy_t0;  // miss streaming start / end (globaltimer ns)
     unsigned long long* copy_t1;
+    unsigned* tiles_done;   // row tiles combined by the down kernel (whole call)
 };
 
 // Device cache state and constants of a handle.
 struct CacheDev {
     int L, E, k, H, I, fmt, has_shared, n_pools, K, norm_topk;
     int pool_mode;               // 0 per layer, 1 shared
+    int fused_upload;            // 1: misses are pulled by the expert kernels themselves
     uint64_t slot_stride, slot_bytes;
     uint8_t* pool;               // [n_pools*K*stride]
     const uint8_t* store;        // mapped pinned store [L*E*stride] (device alias)
@@ -193,6 +207,19 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
+// Programmatic dependent launch: wait for the preceding grid's results, and
+// let the following grid be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+__device__ __forceinline__ void stg_stream(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void stg_stream8(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};\n" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Kernel entry points (launch helpers defined in the .cu files).
 // ---------------------------------------------------------------------------
@@ -203,14 +230,33 @@ struct RouteArgs {
     int T, layer, prefill, bucket;
 };
 
-void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st);
+void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st, bool pdl);
 void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
 void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st);
 void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st);
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
-                   int units, cudaStream_t st);
+                   int units, cudaStream_t st, bool pdl);
 void launch_down(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,
-                 cudaStream_t st);
+                 int bucket, cudaStream_t st, bool pdl);
+
+// cudaLaunchKernelEx with the programmatic-serialization attribute when pdl.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
 size_t route_smem_bytes(const CacheDev& c, int T);
 
 // Host-side repack of canonical records into the slot layout (repack.cpp).

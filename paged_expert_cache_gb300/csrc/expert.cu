@@ -27,24 +27,54 @@ template <> struct Chunk<FMT_FP8_B128> { uint4 q0, q1; float sc; };
 template <> struct Chunk<FMT_BF16> { uint4 q[4]; };
 
 // Loads the lane's share of chunk (rt, kc) of a matrix M (R rows, C cols).
+// When D is not null (a missed expert read from the host store), the same
+// bytes are written to the slot D at the same offsets, so the slot ends up
+// holding the record without a separate copy pass.
 template <int FMT>
-__device__ __forceinline__ void load_chunk(const uint8_t* M, int R, int C, int rt, int kc, int lane, Chunk<FMT>& ch) {
+__device__ __forceinline__ void load_chunk(const uint8_t* M, uint8_t* D, int R, int C, int rt, int kc, int lane,
+                                           Chunk<FMT>& ch) {
     const int KC = C / 64;
     const size_t tile = (size_t)rt * KC + kc;
     if constexpr (FMT == FMT_Q4_0 || FMT == FMT_NVFP4) {
-        ch.q = ldg_stream(M + (tile * 32 + lane) * 16);
-        ch.sc = __ldg(reinterpret_cast<const uint2*>(M + (size_t)R * C / 2 + (tile * 8 + (lane >> 2)) * 8));
+        const size_t qo = (tile * 32 + lane) * 16;
+        const size_t so = (size_t)R * C / 2 + (tile * 8 + (lane >> 2)) * 8;
+        ch.q = ldg_stream(M + qo);
+        if (D) {
+            ch.sc = ldg_stream8(M + so);
+            stg_stream(D + qo, ch.q);
+            if ((lane & 3) == 0) stg_stream8(D + so, ch.sc);
+        } else {
+            ch.sc = __ldg(reinterpret_cast<const uint2*>(M + so));
+        }
     } else if constexpr (FMT == FMT_FP8_B128) {
-        const uint8_t* p = M + (tile * 32 + lane) * 32;
-        ch.q0 = ldg_stream(p);
-        ch.q1 = ldg_stream(p + 16);
+        const size_t qo = (tile * 32 + lane) * 32;
+        ch.q0 = ldg_stream(M + qo);
+        ch.q1 = ldg_stream(M + qo + 16);
         const int nct = (C + 127) / 128;
         ch.sc = __ldg(reinterpret_cast<const float*>(M + (size_t)R * C) + (size_t)((rt * 16) / 128) * nct + (kc * 64) / 128);
+        if (D) {
+            stg_stream(D + qo, ch.q0);
+            stg_stream(D + qo + 16, ch.q1);
+        }
     } else {
-        const uint8_t* p = M + (tile * 32 + lane) * 64;
+        const size_t qo = (tile * 32 + lane) * 64;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ch.q[i] = ldg_stream(p + 16 * i);
+        for (int i = 0; i < 4; ++i) ch.q[i] = ldg_stream(M + qo + 16 * i);
+        if (D) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) stg_stream(D + qo + 16 * i, ch.q[i]);
+        }
     }
+}
+
+// The bytes of a matrix that no lane's chunk covers (block-FP8 tile scales and
+// the padding up to the 16-byte matrix stride), copied by one CTA per matrix.
+template <int FMT>
+__device__ __forceinline__ void copy_matrix_tail(const uint8_t* M, uint8_t* D, int R, int C) {
+    const size_t begin = FMT == FMT_FP8_B128 ? (size_t)R * C : matrix_bytes(FMT, R, C);
+    const size_t end = matrix_stride(FMT, R, C);
+    for (size_t i = begin + threadIdx.x * 4; i < end; i += blockDim.x * 4)
+        *reinterpret_cast<uint32_t*>(D + i) = *reinterpret_cast<const uint32_t*>(M + i);
 }
 
 // acc += A(chunk) * B over the chunk's four k16 steps, for NB B operands
@@ -134,31 +164,73 @@ __device__ __forceinline__ int map_unit(const Plan* p, int has_shared, int kind,
     return u < p->n_uniq ? u : -1;
 }
 
+// The unit of this CTA and its descriptor. For a decode launch (kind 0) the
+// unit index is the CTA's y coordinate, so the descriptor load is issued
+// together with the plan load instead of after it.
+__device__ __forceinline__ int fetch_unit(const Scratch& s, int has_shared, int kind, int group, int G,
+                                          UnitDesc& d) {
+    if (kind == 0) {
+        const int y = blockIdx.y;
+        const int n_units = s.plan->n_units;
+        d = s.units[y];
+        return y < n_units ? y : -1;
+    }
+    const int u = map_unit(s.plan, has_shared, kind, group, G, blockIdx.y);
+    if (u >= 0) d = s.units[u];
+    return u;
+}
+
+__device__ __forceinline__ int pair_at(const Scratch& s, const UnitDesc& d, int i) {
+    if (i >= 8) return s.unit_pairs[d.pstart + i];
+    int r = d.pair8[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+        if (i == j) r = d.pair8[j];  // constant indices keep the descriptor in registers
+    return r;
+}
+
 __device__ __forceinline__ int pair_token(int pair, int T, int k) { return pair < T * k ? pair / k : pair - T * k; }
 
 constexpr int kGUWarps = 8;
 constexpr int kDNWarps = 4;
 constexpr int kMaxChunksInFlight = 4;
 
+__device__ __forceinline__ void note_miss_start(const Scratch& s, const UnitDesc& d) {
+    if (d.dst && threadIdx.x == 0) atomicMin(s.copy_t0, globaltimer_ns());
+}
+__device__ __forceinline__ void note_miss_end(const Scratch& s, const UnitDesc& d) {
+    if (d.dst && threadIdx.x == 0) atomicMax(s.copy_t1, globaltimer_ns());
+}
+
 template <int FMT>
-__global__ void __launch_bounds__(kGUWarps * 32) k_gateup(CacheDev c, Scratch s, const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kGUWarps * 32, (FMT == FMT_Q4_0 || FMT == FMT_NVFP4) ? 3 : (FMT == FMT_FP8_B128 ? 2 : 1)) k_gateup(CacheDev c, Scratch s, const uint16_t* __restrict__ x,
                                                           int T, int kind, int group, int G) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int u = map_unit(s.plan, c.has_shared, kind, group, G, blockIdx.y);
+    griddep_wait();
+    griddep_launch();
+    UnitDesc d;
+    const int u = fetch_unit(s, c.has_shared, kind, group, G, d);
     if (u < 0) return;
+    note_miss_start(s, d);
     const int H = c.H, I = c.I, KC = H / 64, rt = blockIdx.x, k = c.k;
     const int ld = H + 8;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                      // [8][ld]
     float* red = reinterpret_cast<float*>(smem + (size_t)8 * ld * 2);      // [warps][2][128]
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(s.unit_src[u]);
-    const uint64_t mgu = (matrix_bytes(FMT, I, H) + 15) & ~15ull;
-    const uint8_t* Wg = base;
-    const uint8_t* Wu = base + mgu;
-    const float gg = s.unit_g[u * 3], gu = s.unit_g[u * 3 + 1];
-    const int p0 = s.unit_pstart[u], np = s.unit_pstart[u + 1] - p0;
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    const uint8_t* Wg = reinterpret_cast<const uint8_t*>(d.src);
+    const uint8_t* Wu = Wg + mgu;
+    uint8_t* Dg = d.dst ? reinterpret_cast<uint8_t*>(d.dst) : nullptr;
+    uint8_t* Du = Dg ? Dg + mgu : nullptr;
+    if (Dg && rt == 0) {
+        copy_matrix_tail<FMT>(Wg, Dg, I, H);
+        copy_matrix_tail<FMT>(Wu, Du, I, H);
+    }
+    const int np = d.np;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cpw = (KC + kGUWarps - 1) / kGUWarps;
     for (int n0 = 0; n0 < np; n0 += 8) {
+        uint8_t* dg = n0 == 0 ? Dg : nullptr;  // the slot is written on the first pass only
+        uint8_t* du = n0 == 0 ? Du : nullptr;
         float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c0 = 0; c0 < cpw; c0 += kMaxChunksInFlight) {
             Chunk<FMT> cg[kMaxChunksInFlight], cu[kMaxChunksInFlight];
@@ -166,18 +238,19 @@ __global__ void __launch_bounds__(kGUWarps * 32) k_gateup(CacheDev c, Scratch s,
             for (int i = 0; i < kMaxChunksInFlight; ++i) {
                 const int kc = warp * cpw + c0 + i;
                 if (c0 + i < cpw && kc < KC) {
-                    load_chunk<FMT>(Wg, I, H, rt, kc, lane, cg[i]);
-                    load_chunk<FMT>(Wu, I, H, rt, kc, lane, cu[i]);
+                    load_chunk<FMT>(Wg, dg, I, H, rt, kc, lane, cg[i]);
+                    load_chunk<FMT>(Wu, du, I, H, rt, kc, lane, cu[i]);
                 }
             }
             if (c0 == 0) {
                 // stage the tokens while the weight loads are in flight
                 const int vpr = H / 8;
+#pragma unroll 4
                 for (int i = threadIdx.x; i < 8 * vpr; i += blockDim.x) {
                     const int nn = i / vpr, v = i - nn * vpr;
                     uint4 val = make_uint4(0u, 0u, 0u, 0u);
                     if (n0 + nn < np) {
-                        const int t = pair_token(s.unit_pairs[p0 + n0 + nn], T, k);
+                        const int t = pair_token(pair_at(s, d, n0 + nn), T, k);
                         val = *reinterpret_cast<const uint4*>(x + (size_t)t * H + v * 8);
                         if constexpr (FMT != FMT_BF16) {
                             uint32_t w4[4] = {val.x, val.y, val.z, val.w};
@@ -226,50 +299,72 @@ __global__ void __launch_bounds__(kGUWarps * 32) k_gateup(CacheDev c, Scratch s,
                 us += red[(size_t)(w * 2 + 1) * 128 + threadIdx.x];
             }
             if (n0 + col < np) {
-                const int pair = s.unit_pairs[p0 + n0 + col];
-                s.act[(size_t)pair * I + rt * 16 + row] = silu_f(gs * gg) * (us * gu);
+                const int pair = pair_at(s, d, n0 + col);
+                s.act[(size_t)pair * I + rt * 16 + row] = silu_f(gs * d.g[0]) * (us * d.g[1]);
             }
         }
         __syncthreads();
     }
+    note_miss_end(s, d);
 }
 
 template <int FMT>
 __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, float* __restrict__ out, int T,
-                                                        int kind, int group, int G) {
+                                                        int kind, int group, int G, int bucket) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int u = map_unit(s.plan, c.has_shared, kind, group, G, blockIdx.y);
+    griddep_wait();
+    griddep_launch();
+    UnitDesc d;
+    const int u = fetch_unit(s, c.has_shared, kind, group, G, d);
     if (u < 0) return;
+    note_miss_start(s, d);
     const int H = c.H, I = c.I, KC = I / 64, rt = blockIdx.x, k = c.k;
     const int ld = I + 8;
     uint16_t* xh = reinterpret_cast<uint16_t*>(smem);           // [8][ld] activations, high part
     uint16_t* xl = xh + (size_t)8 * ld;                          // [8][ld] low part
     float* red = reinterpret_cast<float*>(xl + (size_t)8 * ld);  // [warps][128]
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(s.unit_src[u]);
-    const uint64_t mgu = (matrix_bytes(FMT, I, H) + 15) & ~15ull;
-    const uint8_t* Wd = base + 2 * mgu;
-    const float gd = s.unit_g[u * 3 + 2];
-    const int p0 = s.unit_pstart[u], np = s.unit_pstart[u + 1] - p0;
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    const uint8_t* Wd = reinterpret_cast<const uint8_t*>(d.src) + 2 * mgu;
+    uint8_t* Dd = d.dst ? reinterpret_cast<uint8_t*>(d.dst) + 2 * mgu : nullptr;
+    if (Dd && rt == 0) copy_matrix_tail<FMT>(Wd, Dd, H, I);
+    const int np = d.np;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cpw = (KC + kDNWarps - 1) / kDNWarps;
     for (int n0 = 0; n0 < np; n0 += 8) {
+        uint8_t* dd = n0 == 0 ? Dd : nullptr;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c0 = 0; c0 < cpw; c0 += kMaxChunksInFlight) {
             Chunk<FMT> cd[kMaxChunksInFlight];
 #pragma unroll
             for (int i = 0; i < kMaxChunksInFlight; ++i) {
                 const int kc = warp * cpw + c0 + i;
-                if (c0 + i < cpw && kc < KC) load_chunk<FMT>(Wd, H, I, rt, kc, lane, cd[i]);
+                if (c0 + i < cpw && kc < KC) load_chunk<FMT>(Wd, dd, H, I, rt, kc, lane, cd[i]);
             }
             if (c0 == 0) {
-                // split each fp32 activation into two 16-bit parts, hi + lo
+                // split each fp32 activation into two 16-bit parts, hi + lo;
+                // all of a thread's loads are issued before any is used
                 const int vpr = I / 4;
-                for (int i = threadIdx.x; i < 8 * vpr; i += blockDim.x) {
+                constexpr int kStage = 12;
+                float4 av4[kStage];
+#pragma unroll
+                for (int r = 0; r < kStage; ++r) {
+                    const int i = threadIdx.x + r * blockDim.x;
+                    const int nn = i / vpr, v = i - nn * vpr;
+                    av4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (i < 8 * vpr && n0 + nn < np)
+                        av4[r] = *reinterpret_cast<const float4*>(s.act + (size_t)pair_at(s, d, n0 + nn) * I + v * 4);
+                }
+                for (int r = 0; r * (int)blockDim.x < 8 * vpr; ++r) {
+                    const int i = threadIdx.x + r * blockDim.x;
+                    if (i >= 8 * vpr) break;
                     const int nn = i / vpr, v = i - nn * vpr;
                     float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (n0 + nn < np) {
-                        const int pair = s.unit_pairs[p0 + n0 + nn];
-                        a4 = *reinterpret_cast<const float4*>(s.act + (size_t)pair * I + v * 4);
+                    if (r < kStage) {
+#pragma unroll
+                        for (int q = 0; q < kStage; ++q)
+                            if (q == r) a4 = av4[q];
+                    } else if (n0 + nn < np) {
+                        a4 = *reinterpret_cast<const float4*>(s.act + (size_t)pair_at(s, d, n0 + nn) * I + v * 4);
                     }
                     const float av[4] = {a4.x, a4.y, a4.z, a4.w};
                     uint16_t hv[4], lv[4];
@@ -318,12 +413,13 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
 #pragma unroll
             for (int w = 0; w < kDNWarps; ++w) sum += red[(size_t)w * 128 + threadIdx.x];
             if (n0 + col < np) {
-                const int pair = s.unit_pairs[p0 + n0 + col];
-                s.part[(size_t)pair * H + rt * 16 + row] = sum * gd;
+                const int pair = pair_at(s, d, n0 + col);
+                s.part[(size_t)pair * H + rt * 16 + row] = sum * d.g[2];
             }
         }
         __syncthreads();
     }
+    note_miss_end(s, d);
     // the CTA that finishes this row tile last combines it for every token
     __threadfence();
     __syncthreads();
@@ -340,7 +436,21 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
         if (c.has_shared) y += __ldcg(s.part + (size_t)(T * k + t) * H + col);
         out[(size_t)t * H + col] = y;
     }
-    if (threadIdx.x == 0) s.tile_done[rt] = 0u;
+    if (threadIdx.x == 0) {
+        s.tile_done[rt] = 0u;
+        // the last row tile of the call books the time misses were streamed
+        if (atomicAdd(s.tiles_done, 1u) == gridDim.x - 1) {
+            __threadfence();
+            const unsigned long long t1 = atomicAdd(s.copy_t1, 0ull);
+            if (t1) {
+                const unsigned long long t0 = atomicAdd(s.copy_t0, 0ull);
+                c.stats[bucket * 5 + 4] += t1 - t0;
+                *s.copy_t0 = ~0ull;
+                *s.copy_t1 = 0ull;
+            }
+            *s.tiles_done = 0u;
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -352,6 +462,7 @@ constexpr int kCopyThreads = 256;
 constexpr uint64_t kCopyChunk = 32768;
 
 __global__ void __launch_bounds__(kCopyThreads) k_copy(CacheDev c, Scratch s, int first, int count, int bucket) {
+    griddep_wait();
     const int n = min(s.plan->n_fill - first, count);
     if (n <= 0) return;
     if (threadIdx.x == 0) atomicMin(s.copy_t0, globaltimer_ns());
@@ -411,7 +522,7 @@ void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int 
 
 template <int FMT>
 static void gateup_fmt(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
-                       int units, cudaStream_t st) {
+                       int units, cudaStream_t st, bool pdl) {
     const size_t sm = (size_t)8 * (c.H + 8) * 2 + (size_t)kGUWarps * 2 * 128 * 4;
     static size_t set = 0;
     if (sm > set) {
@@ -419,12 +530,12 @@ static void gateup_fmt(const CacheDev& c, const Scratch& s, const uint16_t* x, i
         set = sm;
     }
     dim3 grid(c.I / 16, units);
-    k_gateup<FMT><<<grid, kGUWarps * 32, sm, st>>>(c, s, x, T, kind, group, G);
+    launch_ex(k_gateup<FMT>, grid, dim3(kGUWarps * 32), sm, st, pdl, c, s, x, T, kind, group, G);
 }
 
 template <int FMT>
 static void down_fmt(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,
-                     cudaStream_t st) {
+                     int bucket, cudaStream_t st, bool pdl) {
     const size_t sm = (size_t)2 * 8 * (c.I + 8) * 2 + (size_t)kDNWarps * 128 * 4;
     static size_t set = 0;
     if (sm > set) {
@@ -432,26 +543,26 @@ static void down_fmt(const CacheDev& c, const Scratch& s, float* out, int T, int
         set = sm;
     }
     dim3 grid(c.H / 16, units);
-    k_down<FMT><<<grid, kDNWarps * 32, sm, st>>>(c, s, out, T, kind, group, G);
+    launch_ex(k_down<FMT>, grid, dim3(kDNWarps * 32), sm, st, pdl, c, s, out, T, kind, group, G, bucket);
 }
 
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
-                   int units, cudaStream_t st) {
+                   int units, cudaStream_t st, bool pdl) {
     switch (c.fmt) {
-    case FMT_BF16: gateup_fmt<FMT_BF16>(c, s, x, T, kind, group, G, units, st); break;
-    case FMT_Q4_0: gateup_fmt<FMT_Q4_0>(c, s, x, T, kind, group, G, units, st); break;
-    case FMT_FP8_B128: gateup_fmt<FMT_FP8_B128>(c, s, x, T, kind, group, G, units, st); break;
-    case FMT_NVFP4: gateup_fmt<FMT_NVFP4>(c, s, x, T, kind, group, G, units, st); break;
+    case FMT_BF16: gateup_fmt<FMT_BF16>(c, s, x, T, kind, group, G, units, st, pdl); break;
+    case FMT_Q4_0: gateup_fmt<FMT_Q4_0>(c, s, x, T, kind, group, G, units, st, pdl); break;
+    case FMT_FP8_B128: gateup_fmt<FMT_FP8_B128>(c, s, x, T, kind, group, G, units, st, pdl); break;
+    case FMT_NVFP4: gateup_fmt<FMT_NVFP4>(c, s, x, T, kind, group, G, units, st, pdl); break;
     }
 }
 
 void launch_down(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,
-                 cudaStream_t st) {
+                 int bucket, cudaStream_t st, bool pdl) {
     switch (c.fmt) {
-    case FMT_BF16: down_fmt<FMT_BF16>(c, s, out, T, kind, group, G, units, st); break;
-    case FMT_Q4_0: down_fmt<FMT_Q4_0>(c, s, out, T, kind, group, G, units, st); break;
-    case FMT_FP8_B128: down_fmt<FMT_FP8_B128>(c, s, out, T, kind, group, G, units, st); break;
-    case FMT_NVFP4: down_fmt<FMT_NVFP4>(c, s, out, T, kind, group, G, units, st); break;
+    case FMT_BF16: down_fmt<FMT_BF16>(c, s, out, T, kind, group, G, units, bucket, st, pdl); break;
+    case FMT_Q4_0: down_fmt<FMT_Q4_0>(c, s, out, T, kind, group, G, units, bucket, st, pdl); break;
+    case FMT_FP8_B128: down_fmt<FMT_FP8_B128>(c, s, out, T, kind, group, G, units, bucket, st, pdl); break;
+    case FMT_NVFP4: down_fmt<FMT_NVFP4>(c, s, out, T, kind, group, G, units, bucket, st, pdl); break;
     }
 }
 

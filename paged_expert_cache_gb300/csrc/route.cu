@@ -11,11 +11,13 @@
 // order (initial stamps 0..K-1 put slot 0 at the head).
 //
 // Bit-exact top-k. Logits are accumulated per lane with an error-free
-// two-sum (a float pair whose sum carries ~48 bits), so each logit comes with
-// a rigorous bound on its distance from the fp64, ascending-index sum that
-// defines it. When the bound cannot separate the ranking, the candidates are
-// recomputed exactly in that definition's order (sequential fp64, no fused
-// multiply-add) and ranked again.
+// two-sum, so each logit is a normalized float pair (hi, lo) carrying ~48
+// bits, with a rigorous bound on its distance from the fp64, ascending-index
+// sum that defines it. Pairs compare exactly (hi first, then lo) and all the
+// ranking arithmetic stays in fp32: fp64 is slow on this part. Only when the
+// bounds cannot separate the ranking are the candidates recomputed in the
+// definition's own order (sequential fp64, no fused multiply-add) and ranked
+// again.
 #include "common.cuh"
 
 namespace moe {
@@ -33,10 +35,20 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// Logits of one CTA's experts for one CTA's tokens. Writes logits (double)
-// and bounds (double) per (token, expert).
-__device__ void router_logits_tile(const CacheDev& c, const Scratch& s, const RouteArgs& a, uint8_t* smem,
-                                   double* logits, double* bounds) {
+// (a + b) as a normalized pair: s = RN(a + b), e = a + b - s exactly.
+__device__ __forceinline__ float2 norm_pair(float a, float b) {
+    float s, e;
+    two_sum(a, b, s, e);
+    return make_float2(s, e);
+}
+
+// Exact comparison of normalized pairs.
+__device__ __forceinline__ bool pair_gt(float2 a, float2 b) { return a.x > b.x || (a.x == b.x && a.y > b.y); }
+__device__ __forceinline__ bool pair_eq(float2 a, float2 b) { return a.x == b.x && a.y == b.y; }
+
+// Logits of one CTA's experts for one CTA's tokens, with their bounds.
+__device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_t* smem, float2* logits,
+                                   float* bounds) {
     const int H = c.H, E = c.E;
     const int t0 = blockIdx.y * kRouteTokens;
     const int nt = min(kRouteTokens, a.T - t0);
@@ -55,10 +67,18 @@ __device__ void router_logits_tile(const CacheDev& c, const Scratch& s, const Ro
 #pragma unroll
     for (int tt = 0; tt < kRouteTokens; ++tt) hi[tt] = lo[tt] = ab[tt] = 0.f;
     const uint16_t* wr = a.w + (size_t)e * H;
-    for (int cb = lane * 8; cb < H; cb += 256) {
-        uint4 wv = *reinterpret_cast<const uint4*>(wr + cb);
-        float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                       bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+    constexpr int kMaxVec = 16;  // H <= 4096: all of a lane's weight vectors in flight at once
+    const int nvec = H / 256;
+    uint4 wv[kMaxVec];
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i)
+        if (i < nvec) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + lane * 8 + i * 256));
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i) {
+        if (i >= nvec) break;
+        const int cb = lane * 8 + i * 256;
+        float wf[8] = {bf16_lo(wv[i].x), bf16_hi(wv[i].x), bf16_lo(wv[i].y), bf16_hi(wv[i].y),
+                       bf16_lo(wv[i].z), bf16_hi(wv[i].z), bf16_lo(wv[i].w), bf16_hi(wv[i].w)};
 #pragma unroll
         for (int tt = 0; tt < kRouteTokens; ++tt) {
             if (tt < nt) {
@@ -92,22 +112,30 @@ __device__ void router_logits_tile(const CacheDev& c, const Scratch& s, const Ro
             ab[tt] = __fadd_rn(ab[tt], oa);
         }
     }
-    if (lane == 0) {
-        // Bound: the float-pair sum is within g^2 * S of the exact sum (g =
-        // n u / (1 - n u), n the longest chain of roundings, u = 2^-24), the
-        // fp64 definition is within 2048*2^-53 * S plus its bias rounding, and
-        // forming the double costs 2^-53 |z|. Doubled for margin.
-        const double n = (double)(H / 32 + 16);
-        const double g = n * 0x1p-24 / (1.0 - n * 0x1p-24);
-        const double sbound = 0x1p-52 * (double)H;
-        for (int tt = 0; tt < nt; ++tt) {
-            double S = (double)ab[tt] * (1.0 + 2.0 * g);
-            double z = (double)hi[tt] + (double)lo[tt];
-            if (a.bias) z = z + (double)a.bias[e];
-            double beta = 2.0 * (g * g * S + sbound * S + 0x1p-50 * fabs(z)) + (double)H * 0x1p-148 + 1e-300;
-            logits[(size_t)(t0 + tt) * E + e] = z;
-            bounds[(size_t)(t0 + tt) * E + e] = beta;
+    if (lane < nt) {
+        // Bound, all in fp32: the float-pair sum is within g^2 * S of the
+        // exact sum (g = n u / (1 - n u), n the longest chain of roundings,
+        // u = 2^-24, S = sum |x w|); the fp64 definition is within
+        // H * 2^-52 * S of it plus its own bias rounding (2^-52 |z|); folding
+        // the bias into the pair costs at most 2^-46 |z|. Doubled, then
+        // rounded up.
+        const float n = (float)(H / 32 + 16);
+        const float g = n * 0x1p-24f / (1.0f - n * 0x1p-24f);
+        float hv = hi[0], lv = lo[0], av = ab[0];
+#pragma unroll
+        for (int tt = 1; tt < kRouteTokens; ++tt)
+            if (lane == tt) { hv = hi[tt]; lv = lo[tt]; av = ab[tt]; }
+        float2 z = norm_pair(hv, lv);
+        if (a.bias) {
+            float sh, se;
+            two_sum(z.x, a.bias[e], sh, se);
+            z = norm_pair(sh, __fadd_rn(se, z.y));
         }
+        const float S = av * (1.0f + 2.0f * g);
+        const float beta = (2.0f * (g * g * S + (float)H * 0x1p-52f * S + 0x1p-44f * fabsf(z.x)) +
+                            (float)H * 0x1p-126f * 0x1p-22f) * (1.0f + 0x1p-20f);
+        logits[(size_t)(t0 + lane) * E + e] = z;
+        bounds[(size_t)(t0 + lane) * E + e] = beta;
     }
 }
 
@@ -130,135 +158,221 @@ __device__ __forceinline__ bool better(double za, int ea, double zb, int eb) {
     return za > zb || (za == zb && ea < eb);
 }
 
-// Warp-wide argmax by (value desc, index asc) over per-lane candidates.
-__device__ __forceinline__ void warp_best(double& z, int& e) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        double oz = __shfl_xor_sync(0xffffffffu, z, off);
-        int oe = __shfl_xor_sync(0xffffffffu, e, off);
-        if (better(oz, oe, z, e)) { z = oz; e = oe; }
-    }
+__device__ __forceinline__ bool better_pair(float2 za, int ea, float2 zb, int eb) {
+    return pair_gt(za, zb) || (pair_eq(za, zb) && ea < eb);
 }
 
-// Top-k of token t by one warp. zs/bs: per-warp smem of E doubles each,
-// cand: per-warp smem of E ints.
-__device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, const double* logits,
-                           const double* bounds, int t, double* zs, double* bs, int* cand,
-                           unsigned long long* rerank_flag) {
+__device__ __forceinline__ float2 shfl_pair(float2 v, int off) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, off), __shfl_xor_sync(0xffffffffu, v.y, off));
+}
+
+// Per-warp shared memory of the ranking: E entries of each array.
+struct TopkSmem {
+    float2* z;    // logit pairs
+    float* b;     // bounds
+    int* cand;    // re-rank candidates
+    double* z64;  // exact logits of the candidates
+};
+
+__host__ __device__ inline size_t topk_bytes_per_warp(int E) {
+    return (size_t)E * (sizeof(float2) + sizeof(float) + sizeof(int) + sizeof(double));
+}
+
+__device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
+    TopkSmem t;
+    t.z64 = reinterpret_cast<double*>(base);
+    t.z = reinterpret_cast<float2*>(base + (size_t)E * 8);
+    t.b = reinterpret_cast<float*>(base + (size_t)E * 16);
+    t.cand = reinterpret_cast<int*>(base + (size_t)E * 20);
+    return t;
+}
+
+// Top-k of token t by one warp; writes ids and weights of the token.
+__device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
+                           int* rerank_flag) {
     const int E = c.E, k = c.k, lane = threadIdx.x & 31;
     for (int e = lane; e < E; e += 32) {
-        zs[e] = __ldcg(logits + (size_t)t * E + e);
-        bs[e] = __ldcg(bounds + (size_t)t * E + e);
+        w.z[e] = __ldcg(s.logits + (size_t)t * E + e);
+        w.b[e] = __ldcg(s.bounds + (size_t)t * E + e);
     }
     __syncwarp();
     // k rounds of argmax over the untaken experts; bit m of `taken` is e = lane + 32 m
     unsigned taken = 0;
     int sel[kMaxTopK];
-    double selz[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-        double bz = -INFINITY;
-        int be = 0x7fffffff;
-        for (int e = lane, m = 0; e < E; e += 32, ++m)
-            if (!((taken >> m) & 1u) && better(zs[e], e, bz, be)) { bz = zs[e]; be = e; }
-        warp_best(bz, be);
-        sel[j] = be;
-        selz[j] = bz;
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    }
-    // max upper bound over the experts not picked
-    double mx = -INFINITY;
-    for (int e = lane, m = 0; e < E; e += 32, ++m)
-        if (!((taken >> m) & 1u)) mx = fmax(mx, zs[e] + bs[e]);
+    float2 selz[kMaxTopK];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    for (int j = 0; j < kMaxTopK; ++j) {
+        sel[j] = 0;
+        selz[j] = make_float2(0.f, 0.f);
+        if (j < k) {
+            float2 bz = make_float2(-INFINITY, 0.f);
+            int be = 0x7fffffff;
+            for (int e = lane, m = 0; e < E; e += 32, ++m)
+                if (!((taken >> m) & 1u) && better_pair(w.z[e], e, bz, be)) { bz = w.z[e]; be = e; }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                float2 oz = shfl_pair(bz, off);
+                int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                if (better_pair(oz, oe, bz, be)) { bz = oz; be = oe; }
+            }
+            sel[j] = be;
+            selz[j] = bz;
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        }
+    }
+    // largest upper bound (z + b, as a pair) over the experts not picked
+    float2 mx = make_float2(-INFINITY, 0.f);
+    for (int e = lane, m = 0; e < E; e += 32, ++m)
+        if (!((taken >> m) & 1u)) {
+            float2 up = norm_pair(w.z[e].x, __fadd_ru(w.z[e].y, w.b[e]));
+            if (pair_gt(up, mx)) mx = up;
+        }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        float2 o = shfl_pair(mx, off);
+        if (pair_gt(o, mx)) mx = o;
+    }
     // certify: each pick's lower bound is above every later upper bound
     bool ok = true;
-    double run = mx, lam = INFINITY;
-    for (int j = k - 1; j >= 0; --j) {
-        double zj = selz[j], bj = bs[sel[j]];
-        if (!(zj - bj > run)) ok = false;
-        run = fmax(run, zj + bj);
-        lam = fmin(lam, zj - bj);
+    float2 run = mx, lam = make_float2(INFINITY, 0.f);
+#pragma unroll
+    for (int jj = kMaxTopK - 1; jj >= 0; --jj) {
+        if (jj < k) {
+            const float bj = w.b[sel[jj]];
+            const float2 lower = norm_pair(selz[jj].x, __fsub_rd(selz[jj].y, bj));
+            const float2 upper = norm_pair(selz[jj].x, __fadd_ru(selz[jj].y, bj));
+            if (!pair_gt(lower, run)) ok = false;
+            if (pair_gt(upper, run)) run = upper;
+            if (pair_gt(lam, lower)) lam = lower;
+        }
     }
-    int ids[kMaxTopK];
-    double idz[kMaxTopK];
-    for (int j = 0; j < k; ++j) { ids[j] = sel[j]; idz[j] = selz[j]; }
     if (!ok) {
         // candidates: every expert whose upper bound reaches the lowest lower
         // bound of the picks; outside this set no expert can be in the top-k
         int nc = 0;
         for (int base = 0; base < E; base += 32) {
             int e = base + lane;
-            bool in = e < E && zs[e] + bs[e] >= lam;
+            bool in = false;
+            if (e < E) {
+                float2 up = norm_pair(w.z[e].x, __fadd_ru(w.z[e].y, w.b[e]));
+                in = !pair_gt(lam, up);
+            }
             unsigned bal = __ballot_sync(0xffffffffu, in);
-            if (in) cand[nc + __popc(bal & ((1u << lane) - 1u))] = e;
+            if (in) w.cand[nc + __popc(bal & ((1u << lane) - 1u))] = e;
             nc += __popc(bal);
         }
         __syncwarp();
-        for (int i = lane; i < nc; i += 32) zs[cand[i]] = exact_logit(a, c.H, t, cand[i]);
+        for (int i = lane; i < nc; i += 32) w.z64[i] = exact_logit(a, c.H, t, w.cand[i]);
         __syncwarp();
         // k rounds over the candidates; a picked candidate is marked by
         // storing -1 - e in its cand entry
-        for (int j = 0; j < k; ++j) {
-            double bz = -INFINITY;
-            int be = 0x7fffffff, bi = -1;
-            for (int i = lane; i < nc; i += 32) {
-                int e = cand[i];
-                if (e >= 0 && better(zs[e], e, bz, be)) { bz = zs[e]; be = e; bi = i; }
-            }
 #pragma unroll
-            for (int off = 16; off; off >>= 1) {
-                double oz = __shfl_xor_sync(0xffffffffu, bz, off);
-                int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (better(oz, oe, bz, be)) { bz = oz; be = oe; bi = oi; }
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k) {
+                double bz = -INFINITY;
+                int be = 0x7fffffff, bi = -1;
+                for (int i = lane; i < nc; i += 32) {
+                    int e = w.cand[i];
+                    if (e >= 0 && better(w.z64[i], e, bz, be)) { bz = w.z64[i]; be = e; bi = i; }
+                }
+#pragma unroll
+                for (int off = 16; off; off >>= 1) {
+                    double oz = __shfl_xor_sync(0xffffffffu, bz, off);
+                    int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                    int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    if (better(oz, oe, bz, be)) { bz = oz; be = oe; bi = oi; }
+                }
+                sel[j] = be;
+                selz[j] = w.z[be];
+                if (lane == (bi & 31)) w.cand[bi] = -1 - be;
+                __syncwarp();
             }
-            ids[j] = be;
-            idz[j] = bz;
-            if (lane == (bi & 31)) cand[bi] = -1 - be;
-            __syncwarp();
         }
-        if (lane == 0) atomicExch(rerank_flag, 1ull);
+        if (lane == 0) *rerank_flag = 1;
     }
     // combine weights in fp32 from the picks' logits
-    if (lane == 0) {
-        float w[kMaxTopK];
-        float sum = 0.f;
-        if (c.norm_topk) {
-            for (int j = 0; j < k; ++j) { w[j] = expf((float)(idz[j] - idz[0])); sum += w[j]; }
-        } else {
-            double zmax = -INFINITY;
-            for (int e = 0; e < E; ++e) zmax = fmax(zmax, zs[e]);
-            for (int e = 0; e < E; ++e) sum += expf((float)(zs[e] - zmax));
-            for (int j = 0; j < k; ++j) w[j] = expf((float)(idz[j] - zmax));
-        }
-        for (int j = 0; j < k; ++j) {
-            s.ids[t * k + j] = ids[j];
-            s.wts[t * k + j] = w[j] / sum;
+    float sum = 0.f;
+    float zref = selz[0].x;
+    if (!c.norm_topk) {
+        float zmax = -INFINITY;
+        for (int e = lane; e < E; e += 32) zmax = fmaxf(zmax, w.z[e].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
+        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zmax);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        zref = zmax;
+    } else {
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k) zref = fmaxf(zref, selz[j].x);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k) sum += expf(selz[j].x - zref);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k && lane == (j & 31)) {
+            s.ids[t * k + j] = sel[j];
+            s.wts[t * k + j] = expf(selz[j].x - zref) / sum;
         }
     }
     __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// Plan of a decode call (T <= 32): the cache transaction, run by one CTA.
+// Plan of a decode call (T <= 32): the cache transaction, run by one CTA on
+// a copy of the pool's state held in shared memory.
 // ---------------------------------------------------------------------------
 struct PlanSmem {
-    int* first;       // [E] first pair index routed to e (or INT_MAX)
-    int* unit_of;     // [E]
-    unsigned* missbits;  // [E/32 + 1]
-    int* u_expert;    // [U]
-    int* u_slot;      // [U]
-    int* u_hit;       // [U]
-    int* u_cnt;       // [U+1]
-    int* p_unit;      // [P]
     unsigned long long* lu;  // [K] last-use stamps of the pool
-    unsigned long long* wmin;  // [8]
-    int* wslot;       // [8]
-    int* victims;     // [U]
-    int* misses;      // [U] miss experts ascending
-    int* scal;        // [8]: 0 n_uniq, 1 n_hit, 2 n_miss
+    int* kof;                // [K] keys of the pool's slots
+    int* smap;               // [E] slot map of the layer
+    int* first;              // [E] first pair index routed to e
+    int* unit_of;            // [E]
+    unsigned* missbits;      // [E/32 + 1]
+    int* u_expert;           // [U]
+    int* u_slot;             // [U]
+    int* u_hit;              // [U]
+    int* u_cnt;              // [U+1]
+    int* p_unit;             // [P]
+    int* victims;            // [U]
+    int* misses;             // [U] miss experts ascending
+    int* ids;                // [T*k] this call's picks
+    unsigned long long* wmin;  // [32]
+    int* wslot;              // [32]
+    int* scal;               // [8]
+    size_t bytes;
 };
+
+__host__ __device__ inline PlanSmem plan_layout(uint8_t* base, int E, int K, int n_ids, int U, int P) {
+    PlanSmem m;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* q = base + off;
+        off += (bytes + 15) & ~(size_t)15;
+        return q;
+    };
+    m.lu = (unsigned long long*)take(sizeof(unsigned long long) * K);
+    m.kof = (int*)take(sizeof(int) * K);
+    m.smap = (int*)take(sizeof(int) * E);
+    m.first = (int*)take(sizeof(int) * E);
+    m.unit_of = (int*)take(sizeof(int) * E);
+    m.missbits = (unsigned*)take(sizeof(unsigned) * (E / 32 + 1));
+    m.u_expert = (int*)take(sizeof(int) * U);
+    m.u_slot = (int*)take(sizeof(int) * U);
+    m.u_hit = (int*)take(sizeof(int) * U);
+    m.u_cnt = (int*)take(sizeof(int) * (U + 1));
+    m.p_unit = (int*)take(sizeof(int) * P);
+    m.victims = (int*)take(sizeof(int) * U);
+    m.misses = (int*)take(sizeof(int) * U);
+    m.ids = (int*)take(sizeof(int) * n_ids);
+    m.wmin = (unsigned long long*)take(sizeof(unsigned long long) * 32);
+    m.wslot = (int*)take(sizeof(int) * 32);
+    m.scal = (int*)take(sizeof(int) * 8);
+    m.bytes = off;
+    return m;
+}
 
 __device__ void write_trace(const CacheDev& c, const Scratch& s, int layer, int T, int n_ids, int n_hit,
                             int n_fill, int n_uniq) {
@@ -281,85 +395,78 @@ __device__ void write_trace(const CacheDev& c, const Scratch& s, int layer, int 
     *c.trace_count = idx + 1;
 }
 
-__device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs& a, uint8_t* smem) {
+__device__ void plan_prefetch(const CacheDev& c, const RouteArgs& a, const PlanSmem& m, int pool) {
+    const unsigned long long* lu = c.last_use + (size_t)pool * c.K;
+    const int* kof = c.key_of + (size_t)pool * c.K;
+    const int* smap = c.slot_map + (size_t)a.layer * c.E;
+    for (int i = threadIdx.x; i < c.K; i += blockDim.x) {
+        m.lu[i] = lu[i];
+        m.kof[i] = kof[i];
+    }
+    for (int e = threadIdx.x; e < c.E; e += blockDim.x) {
+        m.smap[e] = smap[e];
+        m.first[e] = 0x7fffffff;
+    }
+    for (int i = threadIdx.x; i <= c.E / 32; i += blockDim.x) m.missbits[i] = 0u;
+}
+
+__device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs& a, const PlanSmem& m,
+                            unsigned long long clk) {
     const int E = c.E, k = c.k, T = a.T, layer = a.layer;
     const int n_ids = T * k;
     const int pool = c.pool_mode ? 0 : layer;
     const int K = c.K;
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const int U = min(n_ids, E) + 1;
     const int P = n_ids + (c.has_shared ? T : 0);
-    PlanSmem m;
-    uint8_t* p = smem;
-    auto take = [&](size_t bytes) { uint8_t* q = p; p += (bytes + 15) & ~(size_t)15; return q; };
-    m.first = (int*)take(sizeof(int) * E);
-    m.unit_of = (int*)take(sizeof(int) * E);
-    m.missbits = (unsigned*)take(sizeof(unsigned) * (E / 32 + 1));
-    m.u_expert = (int*)take(sizeof(int) * U);
-    m.u_slot = (int*)take(sizeof(int) * U);
-    m.u_hit = (int*)take(sizeof(int) * U);
-    m.u_cnt = (int*)take(sizeof(int) * (U + 1));
-    m.p_unit = (int*)take(sizeof(int) * P);
-    m.victims = (int*)take(sizeof(int) * U);
-    m.misses = (int*)take(sizeof(int) * U);
-    m.wmin = (unsigned long long*)take(sizeof(unsigned long long) * 32);
-    m.wslot = (int*)take(sizeof(int) * 32);
-    m.scal = (int*)take(sizeof(int) * 8);
-    m.lu = (unsigned long long*)take(sizeof(unsigned long long) * K);
-
-    int* slot_map = c.slot_map + (size_t)layer * E;
-    int* key_of = c.key_of + (size_t)pool * K;
-    unsigned long long* last_use = c.last_use + (size_t)pool * K;
+    int* g_slot_map = c.slot_map + (size_t)layer * E;
+    int* g_key_of = c.key_of + (size_t)pool * K;
+    unsigned long long* g_last_use = c.last_use + (size_t)pool * K;
 
     // 1. dedupe: first occurrence in [token][rank] order
-    for (int e = tid; e < E; e += nthr) m.first[e] = 0x7fffffff;
-    for (int i = tid; i <= E / 32; i += nthr) m.missbits[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n_ids; i += nthr) atomicMin(&m.first[s.ids[i]], i);
+    for (int i = tid; i < n_ids; i += nthr) {
+        int e = s.ids[i];
+        m.ids[i] = e;
+        atomicMin(&m.first[e], i);
+    }
     __syncthreads();
     if (tid < 32) {
-        // unit index = rank of the first occurrence among first occurrences
         int base = 0;
         for (int i0 = 0; i0 < n_ids; i0 += 32) {
             int i = i0 + tid;
-            bool f = i < n_ids && m.first[s.ids[i]] == i;
+            bool f = i < n_ids && m.first[m.ids[i]] == i;
             unsigned bal = __ballot_sync(0xffffffffu, f);
             if (f) {
                 int u = base + __popc(bal & ((1u << tid) - 1u));
-                m.unit_of[s.ids[i]] = u;
-                m.u_expert[u] = s.ids[i];
+                m.unit_of[m.ids[i]] = u;
+                m.u_expert[u] = m.ids[i];
             }
             base += __popc(bal);
         }
-        if (tid == 0) m.scal[0] = base;
-    }
-    __syncthreads();
-    const int nu = m.scal[0];
-    // 2. hits: touched in unit order, stamps clock + hit rank
-    const unsigned long long clk = c.clock[pool];
-    if (tid < 32) {
-        int base = 0;
+        __syncwarp();
+        const int nu = base;
+        // 2. hits, touched in unit order: stamps clock + hit rank
+        int hb = 0;
         for (int u0 = 0; u0 < nu; u0 += 32) {
             int u = u0 + tid;
-            int sl = u < nu ? slot_map[m.u_expert[u]] : -1;
+            int sl = u < nu ? m.smap[m.u_expert[u]] : -1;
             bool h = sl >= 0;
             unsigned bal = __ballot_sync(0xffffffffu, h);
             if (u < nu) {
                 m.u_hit[u] = h;
                 m.u_slot[u] = sl;
-                if (h) last_use[sl] = clk + base + __popc(bal & ((1u << tid) - 1u));
-                else atomicOr(&m.missbits[m.u_expert[u] >> 5], 1u << (m.u_expert[u] & 31));
+                if (h) {
+                    unsigned long long st = clk + hb + __popc(bal & ((1u << tid) - 1u));
+                    m.lu[sl] = st;
+                    g_last_use[sl] = st;
+                } else {
+                    atomicOr(&m.missbits[m.u_expert[u] >> 5], 1u << (m.u_expert[u] & 31));
+                }
             }
-            base += __popc(bal);
+            hb += __popc(bal);
         }
-        if (tid == 0) m.scal[1] = base;
-    }
-    __syncthreads();
-    const int nh = m.scal[1];
-    const int nmiss = nu - nh;
-    // misses in ascending expert order
-    if (tid < 32) {
-        int base = 0;
+        __syncwarp();
+        // misses in ascending expert order
+        int mb = 0;
         for (int w0 = 0; w0 <= E / 32; w0 += 32) {
             int wi = w0 + tid;
             unsigned bits = wi <= E / 32 ? m.missbits[wi] : 0u;
@@ -370,18 +477,24 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
                 int v = __shfl_up_sync(0xffffffffu, incl, off);
                 if (tid >= off) incl += v;
             }
-            int pos = base + incl - cnt;
+            int pos = mb + incl - cnt;
             while (bits) {
                 int b = __ffs(bits) - 1;
                 bits &= bits - 1;
                 m.misses[pos++] = wi * 32 + b;
             }
-            base += __shfl_sync(0xffffffffu, incl, 31);
+            mb += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (tid == 0) {
+            m.scal[0] = nu;
+            m.scal[1] = hb;
         }
     }
-    // 3. victims: the nmiss smallest stamps of the pool, smallest first
-    for (int i = tid; i < K; i += nthr) m.lu[i] = last_use[i];
     __syncthreads();
+    const int nu = m.scal[0];
+    const int nh = m.scal[1];
+    const int nmiss = nu - nh;
+    // 3. victims: the nmiss smallest stamps of the pool, smallest first
     if (nmiss > 0) {
         unsigned long long myv = ~0ull;
         int mys = -1;
@@ -408,8 +521,7 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
                 m.lu[bsl] = ~0ull;
             }
             __syncthreads();
-            int taken = m.victims[r];
-            if (taken == mys) {
+            if (m.victims[r] == mys) {
                 myv = ~0ull;
                 mys = -1;
                 for (int i = tid; i < K; i += nthr)
@@ -422,37 +534,41 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
     for (int i = tid; i < nmiss; i += nthr) {
         int e = m.misses[i];
         int v = m.victims[i];
-        int old = key_of[v];
+        int old = m.kof[v];
         if (old >= 0) c.slot_map[old] = -1;
-        key_of[v] = layer * E + e;
-        slot_map[e] = v;
-        last_use[v] = clk + nh + i;
+        g_key_of[v] = layer * E + e;
+        g_slot_map[e] = v;
+        g_last_use[v] = clk + nh + i;
         m.u_slot[m.unit_of[e]] = v;
         s.copy_expert[i] = e;
         s.copy_slot[i] = v;
-        s.copy_src[i] = (uint64_t)(c.store + ((size_t)layer * E + e) * c.slot_stride);
-        s.copy_dst[i] = (uint64_t)(c.pool + ((size_t)pool * K + v) * c.slot_stride);
     }
-    __syncthreads();
-    // 5. units and pairs
+    // 5. units and their pairs
     const int n_units = nu + (c.has_shared ? 1 : 0);
     for (int u = tid; u <= n_units; u += nthr) m.u_cnt[u] = 0;
     __syncthreads();
     for (int i = tid; i < P; i += nthr) {
-        int u = i < n_ids ? m.unit_of[s.ids[i]] : nu;
+        int u = i < n_ids ? m.unit_of[m.ids[i]] : nu;
         m.p_unit[i] = u;
         atomicAdd(&m.u_cnt[u], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int u = 0; u < n_units; ++u) {
-            int cnt = m.u_cnt[u];
-            s.unit_pstart[u] = acc;
-            m.u_cnt[u] = acc;
-            acc += cnt;
+    if (tid < 32) {
+        // exclusive prefix over the unit counts
+        int base = 0;
+        for (int u0 = 0; u0 < n_units; u0 += 32) {
+            int u = u0 + tid;
+            int cnt = u < n_units ? m.u_cnt[u] : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (tid >= off) incl += v;
+            }
+            if (u < n_units) m.u_cnt[u] = base + incl - cnt;
+            base += __shfl_sync(0xffffffffu, incl, 31);
         }
-        s.unit_pstart[n_units] = acc;
+        if (tid == 0) m.u_cnt[n_units] = base;
     }
     __syncthreads();
     for (int i = tid; i < P; i += nthr) {
@@ -462,22 +578,41 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
         s.unit_pairs[m.u_cnt[u] + pos] = i;
         s.pair_unit[i] = u;
     }
+    __syncthreads();
     for (int u = tid; u < n_units; u += nthr) {
+        UnitDesc d;
+        d.pstart = m.u_cnt[u];
+        d.np = m.u_cnt[u + 1] - m.u_cnt[u];
+        for (int j = 0; j < 8; ++j) d.pair8[j] = -1;
+        for (int i = 0, got = 0; i < P && got < 8 && got < d.np; ++i)
+            if (m.p_unit[i] == u) d.pair8[got++] = i;
         if (u < nu) {
-            int e = m.u_expert[u];
-            s.unit_expert[u] = e;
-            s.unit_slot[u] = m.u_slot[u];
-            s.unit_src[u] = (uint64_t)(c.pool + ((size_t)pool * K + m.u_slot[u]) * c.slot_stride);
-            for (int j = 0; j < 3; ++j) s.unit_g[u * 3 + j] = c.gtable[((size_t)layer * E + e) * 3 + j];
+            const int e = m.u_expert[u];
+            const int sl = m.u_slot[u];
+            const uint64_t slot_addr = (uint64_t)(c.pool + ((size_t)pool * K + sl) * c.slot_stride);
+            d.expert = e;
+            d.slot = sl;
+            d.hit = m.u_hit[u];
+            if (!d.hit && c.fused_upload) {
+                d.src = (uint64_t)(c.store + ((size_t)layer * E + e) * c.slot_stride);
+                d.dst = slot_addr;
+            } else {
+                d.src = slot_addr;
+                d.dst = 0;
+            }
+            for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)layer * E + e) * 3 + j];
         } else {
-            s.unit_expert[u] = -1;
-            s.unit_slot[u] = -1;
-            s.unit_src[u] = (uint64_t)(c.shared_w + (size_t)layer * c.slot_stride);
-            for (int j = 0; j < 3; ++j) s.unit_g[u * 3 + j] = c.gtable[((size_t)c.L * E + layer) * 3 + j];
+            d.expert = -1;
+            d.slot = -1;
+            d.hit = 1;
+            d.src = (uint64_t)(c.shared_w + (size_t)layer * c.slot_stride);
+            d.dst = 0;
+            for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)c.L * E + layer) * 3 + j];
         }
+        s.units[u] = d;
     }
     for (int i = tid; i < n_ids; i += nthr) {
-        int u = m.unit_of[s.ids[i]];
+        int u = m.unit_of[m.ids[i]];
         s.slot_of[i] = m.u_slot[u];
         s.hit_of[i] = m.u_hit[u];
     }
@@ -500,55 +635,58 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
 }
 
 // Fused decode routing: all CTAs compute logits; the last CTA to finish
-// ranks every token and runs the plan.
+// prefetches the pool's state, ranks every token and runs the plan.
 __global__ void __launch_bounds__(kRouteThreads) k_route(CacheDev c, Scratch s, RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    double* logits = s.logits;
-    double* bounds = s.bounds;
-    router_logits_tile(c, s, a, smem, logits, bounds);
+    griddep_wait();
+    griddep_launch();
+    router_logits_tile(c, a, smem, s.logits, s.bounds);
     if (a.prefill) return;
     __threadfence();
     __syncthreads();
     __shared__ int is_last;
+    __shared__ int rerank;
+    __shared__ unsigned long long clk;
     if (threadIdx.x == 0) {
         unsigned total = gridDim.x * gridDim.y;
         is_last = atomicAdd(s.route_done, 1u) == total - 1;
+        rerank = 0;
     }
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    const int E = c.E, T = a.T, n_ids = T * c.k;
+    const int U = min(n_ids, E) + 1;
+    const int P = n_ids + (c.has_shared ? T : 0);
+    const int pool = c.pool_mode ? 0 : a.layer;
+    PlanSmem m = plan_layout(smem, E, c.K, n_ids, U, P);
+    plan_prefetch(c, a, m, pool);  // overlaps the ranking below
+    if (threadIdx.x == 0) clk = c.clock[pool];
     const int warp = threadIdx.x >> 5;
-    const int E = c.E;
-    __shared__ unsigned long long rerank;
-    if (threadIdx.x == 0) rerank = 0;
-    __syncthreads();
-    double* zs = reinterpret_cast<double*>(smem) + (size_t)warp * 2 * E;
-    double* bs = zs + E;
-    int* cand = reinterpret_cast<int*>(reinterpret_cast<double*>(smem) + (size_t)kRouteWarps * 2 * E) + warp * E;
-    for (int t = warp; t < a.T; t += kRouteWarps) topk_token(c, s, a, logits, bounds, t, zs, bs, cand, &rerank);
+    const int nwt = min(kRouteWarps, T);
+    const TopkSmem tw = topk_layout(smem + m.bytes + (size_t)warp * topk_bytes_per_warp(E), E);
+    if (warp < nwt)
+        for (int t = warp; t < T; t += nwt) topk_token(c, s, a, t, tw, &rerank);
     __syncthreads();
     if (threadIdx.x == 0) {
         *s.route_done = 0;
-        if (rerank) { c.stats[15] += 1; s.plan->reranked = 1; } else s.plan->reranked = 0;
+        s.plan->reranked = rerank;
+        if (rerank) c.stats[15] += 1;
     }
-    __syncthreads();
-    plan_decode(c, s, a, smem);
+    plan_decode(c, s, a, m, clk);
 }
 
 // Prefill: one warp per token.
 __global__ void __launch_bounds__(kRouteThreads) k_topk(CacheDev c, Scratch s, RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait();
     const int warp = threadIdx.x >> 5, E = c.E;
     const int t = blockIdx.x * kRouteWarps + warp;
-    __shared__ unsigned long long rerank;
+    __shared__ int rerank;
     if (threadIdx.x == 0) rerank = 0;
     __syncthreads();
-    double* zs = reinterpret_cast<double*>(smem) + (size_t)warp * 2 * E;
-    double* bs = zs + E;
-    int* cand = reinterpret_cast<int*>(reinterpret_cast<double*>(smem) + (size_t)kRouteWarps * 2 * E) + warp * E;
-    if (t < a.T)
-        topk_token(c, s, a, s.logits, s.bounds, t, zs, bs,
-                   cand, &rerank);
+    const TopkSmem tw = topk_layout(smem + (size_t)warp * topk_bytes_per_warp(E), E);
+    if (t < a.T) topk_token(c, s, a, t, tw, &rerank);
     __syncthreads();
     if (threadIdx.x == 0 && rerank) atomicAdd(c.stats + 15, 1ull);
 }
@@ -557,16 +695,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk(CacheDev c, Scratch s, R
 // staged experts ascending (so groups of `group` are contiguous ranges).
 __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, RouteArgs a, int group) {
     extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait();
     const int E = c.E, k = c.k, T = a.T, layer = a.layer;
     const int n_ids = T * k;
     const int P = n_ids + (c.has_shared ? T : 0);
     const int tid = threadIdx.x, nthr = blockDim.x;
     int* used = reinterpret_cast<int*>(smem);  // [E]
     int* unit_of = used + E;                   // [E]
-    int* cnt = unit_of + E;                    // [E+1]
-    int* cur = cnt + E + 1;                    // [E+1]
+    int* cnt = unit_of + E;                    // [E+2]
+    int* cur = cnt + E + 2;                    // [E+2]
     __shared__ int nh_s, nu_s;
-    int* slot_map = c.slot_map + (size_t)layer * E;
+    const int* slot_map = c.slot_map + (size_t)layer * E;
+    const int pool = c.pool_mode ? 0 : layer;
     for (int e = tid; e < E; e += nthr) used[e] = 0;
     __syncthreads();
     for (int i = tid; i < n_ids; i += nthr) used[s.ids[i]] = 1;
@@ -593,23 +733,6 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
     __syncthreads();
     const int nu = nu_s, nh = nh_s;
     const int n_units = nu + (c.has_shared ? 1 : 0);
-    for (int e = tid; e < E; e += nthr) {
-        if (!used[e]) continue;
-        int u = unit_of[e];
-        bool hit = slot_map[e] >= 0;
-        s.unit_expert[u] = e;
-        s.unit_slot[u] = hit ? slot_map[e] : -1;
-        int pool = c.pool_mode ? 0 : layer;
-        s.unit_src[u] = hit ? (uint64_t)(c.pool + ((size_t)pool * c.K + slot_map[e]) * c.slot_stride)
-                            : s.copy_dst[u - nh];
-        for (int j = 0; j < 3; ++j) s.unit_g[u * 3 + j] = c.gtable[((size_t)layer * E + e) * 3 + j];
-    }
-    if (tid == 0 && c.has_shared) {
-        s.unit_expert[nu] = -1;
-        s.unit_slot[nu] = -1;
-        s.unit_src[nu] = (uint64_t)(c.shared_w + (size_t)layer * c.slot_stride);
-        for (int j = 0; j < 3; ++j) s.unit_g[nu * 3 + j] = c.gtable[((size_t)c.L * E + layer) * 3 + j];
-    }
     for (int u = tid; u <= n_units; u += nthr) cnt[u] = 0;
     __syncthreads();
     for (int i = tid; i < P; i += nthr) {
@@ -621,16 +744,48 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
     if (tid == 0) {
         int acc = 0;
         for (int u = 0; u < n_units; ++u) {
-            s.unit_pstart[u] = acc;
             cur[u] = acc;
             acc += cnt[u];
         }
-        s.unit_pstart[n_units] = acc;
+        cur[n_units] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += nthr) {
+        if (!used[e]) continue;
+        const int u = unit_of[e];
+        const bool hit = slot_map[e] >= 0;
+        UnitDesc d;
+        d.pstart = cur[u];
+        d.np = cnt[u];
+        d.expert = e;
+        d.slot = hit ? slot_map[e] : -1;
+        d.hit = hit;
+        d.src = hit ? (uint64_t)(c.pool + ((size_t)pool * c.K + slot_map[e]) * c.slot_stride) : s.copy_dst[u - nh];
+        d.dst = 0;
+        for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)layer * E + e) * 3 + j];
+        s.units[u] = d;
+    }
+    if (tid == 0 && c.has_shared) {
+        UnitDesc d;
+        d.pstart = cur[nu];
+        d.np = cnt[nu];
+        d.expert = -1;
+        d.slot = -1;
+        d.hit = 1;
+        d.src = (uint64_t)(c.shared_w + (size_t)layer * c.slot_stride);
+        d.dst = 0;
+        for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)c.L * E + layer) * 3 + j];
+        s.units[nu] = d;
     }
     __syncthreads();
     for (int i = tid; i < P; i += nthr) {
         int u = s.pair_unit[i];
         s.unit_pairs[atomicAdd(&cur[u], 1)] = i;
+    }
+    __syncthreads();
+    for (int u = tid; u < n_units; u += nthr) {
+        const int st = s.units[u].pstart, n = s.units[u].np;
+        for (int j = 0; j < 8; ++j) s.units[u].pair8[j] = j < n ? s.unit_pairs[st + j] : -1;
     }
     for (int i = tid; i < n_ids; i += nthr) {
         int e = s.ids[i];
@@ -657,37 +812,19 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
-static size_t topk_smem(int E) { return (size_t)kRouteWarps * E * (2 * sizeof(double) + sizeof(int)); }
-
-static size_t plan_smem(const CacheDev& c, int T) {
-    int n_ids = T * c.k;
-    int U = min(n_ids, c.E) + 1;
-    int P = n_ids + (c.has_shared ? T : 0);
-    size_t b = 0;
-    auto add = [&](size_t x) { b += (x + 15) & ~(size_t)15; };
-    add(sizeof(int) * c.E);
-    add(sizeof(int) * c.E);
-    add(sizeof(unsigned) * (c.E / 32 + 1));
-    for (int i = 0; i < 4; ++i) add(sizeof(int) * (U + 1));
-    add(sizeof(int) * P);
-    add(sizeof(int) * U);
-    add(sizeof(int) * U);
-    add(sizeof(unsigned long long) * 32);
-    add(sizeof(int) * 32);
-    add(sizeof(int) * 8);
-    add(sizeof(unsigned long long) * c.K);
-    return b;
-}
+static size_t topk_smem(int E, int warps) { return (size_t)warps * topk_bytes_per_warp(E); }
 
 size_t route_smem_bytes(const CacheDev& c, int T) {
+    const int n_ids = T * c.k;
+    const int U = min(n_ids, c.E) + 1;
+    const int P = n_ids + (c.has_shared ? T : 0);
     size_t x = (size_t)kRouteTokens * c.H * sizeof(uint16_t);
-    size_t tk = topk_smem(c.E);
-    size_t pl = plan_smem(c, T);
-    size_t m = x > tk ? x : tk;
-    return m > pl ? m : pl;
+    size_t last = plan_layout(nullptr, c.E, c.K, n_ids, U, P).bytes + topk_smem(c.E, min(kRouteWarps, T));
+    return x > last ? x : last;
 }
 
-void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /*max_units*/, cudaStream_t st) {
+void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /*max_units*/, cudaStream_t st,
+                  bool pdl) {
     dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (a.T + kRouteTokens - 1) / kRouteTokens);
     size_t sm = a.prefill ? (size_t)kRouteTokens * c.H * sizeof(uint16_t) : route_smem_bytes(c, a.T);
     static size_t set_route = 0;
@@ -695,11 +832,11 @@ void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /
         cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         set_route = sm;
     }
-    k_route<<<grid, kRouteThreads, sm, st>>>(c, s, a);
+    launch_ex(k_route, grid, dim3(kRouteThreads), sm, st, pdl, c, s, a);
 }
 
 void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st) {
-    size_t sm = topk_smem(c.E);
+    size_t sm = topk_smem(c.E, kRouteWarps);
     static size_t set_topk = 0;
     if (sm > set_topk) {
         cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -709,7 +846,7 @@ void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a
 }
 
 void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st) {
-    size_t sm = sizeof(int) * (4 * (size_t)c.E + 2);
+    size_t sm = sizeof(int) * (4 * (size_t)c.E + 4);
     static size_t set_plan = 0;
     if (sm > set_plan) {
         cudaFuncSetAttribute(k_plan_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
