@@ -417,7 +417,10 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
             }
         }
         timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 0, 0, h->G, units, st, pdl); });
-        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, bucket, st, pdl); });
+        timed(h, 3, st, [&] {
+            if (!moe::launch_down_rows(d, h->scr, out, T, units, bucket, st, pdl))
+                moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, bucket, st, pdl);
+        });
     } else {
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, false); });
         timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });

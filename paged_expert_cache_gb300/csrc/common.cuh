@@ -258,6 +258,8 @@ inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 size_t route_smem_bytes(const CacheDev& c, int T);
+bool launch_down_rows(const CacheDev& c, const Scratch& s, float* out, int T, int units, int bucket, cudaStream_t st,
+                      bool pdl);
 
 // Host-side repack of canonical records into the slot layout (repack.cpp).
 void repack_record(int fmt, int H, int I, const uint8_t* canonical, uint8_t* slot, float* gscales3);

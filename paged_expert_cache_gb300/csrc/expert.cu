@@ -305,6 +305,30 @@ __global__ void __launch_bounds__(kGUWarps * 32, (FMT == FMT_Q4_0 || FMT == FMT_
         }
         __syncthreads();
     }
+    if (Dg) {
+        // this CTA's share of the missed record's down projection goes to the
+        // slot now, so the whole record crosses the host link in one kernel
+        // and the down kernel reads it from device memory
+        const uint64_t mdn = matrix_stride(FMT, H, I);
+        const uint64_t nvec = mdn / 16, per = (nvec + gridDim.x - 1) / gridDim.x;
+        const uint64_t v0 = (uint64_t)rt * per, v1 = v0 + per < nvec ? v0 + per : nvec;
+        const uint8_t* src = Wg + 2 * mgu;
+        uint8_t* dst = Dg + 2 * mgu;
+        constexpr int kBatch = 4;
+        for (uint64_t v = v0 + threadIdx.x; v < v1; v += (uint64_t)blockDim.x * kBatch) {
+            uint4 buf[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const uint64_t vi = v + (uint64_t)i * blockDim.x;
+                if (vi < v1) buf[i] = ldg_stream(src + vi * 16);
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const uint64_t vi = v + (uint64_t)i * blockDim.x;
+                if (vi < v1) stg_stream(dst + vi * 16, buf[i]);
+            }
+        }
+    }
     note_miss_end(s, d);
 }
 
@@ -317,28 +341,25 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
     UnitDesc d;
     const int u = fetch_unit(s, c.has_shared, kind, group, G, d);
     if (u < 0) return;
-    note_miss_start(s, d);
     const int H = c.H, I = c.I, KC = I / 64, rt = blockIdx.x, k = c.k;
     const int ld = I + 8;
     uint16_t* xh = reinterpret_cast<uint16_t*>(smem);           // [8][ld] activations, high part
     uint16_t* xl = xh + (size_t)8 * ld;                          // [8][ld] low part
     float* red = reinterpret_cast<float*>(xl + (size_t)8 * ld);  // [warps][128]
     const uint64_t mgu = matrix_stride(FMT, I, H);
-    const uint8_t* Wd = reinterpret_cast<const uint8_t*>(d.src) + 2 * mgu;
-    uint8_t* Dd = d.dst ? reinterpret_cast<uint8_t*>(d.dst) + 2 * mgu : nullptr;
-    if (Dd && rt == 0) copy_matrix_tail<FMT>(Wd, Dd, H, I);
+    // a missed expert was written to its slot by the gate/up kernel
+    const uint8_t* Wd = reinterpret_cast<const uint8_t*>(d.dst ? d.dst : d.src) + 2 * mgu;
     const int np = d.np;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cpw = (KC + kDNWarps - 1) / kDNWarps;
     for (int n0 = 0; n0 < np; n0 += 8) {
-        uint8_t* dd = n0 == 0 ? Dd : nullptr;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c0 = 0; c0 < cpw; c0 += kMaxChunksInFlight) {
             Chunk<FMT> cd[kMaxChunksInFlight];
 #pragma unroll
             for (int i = 0; i < kMaxChunksInFlight; ++i) {
                 const int kc = warp * cpw + c0 + i;
-                if (c0 + i < cpw && kc < KC) load_chunk<FMT>(Wd, dd, H, I, rt, kc, lane, cd[i]);
+                if (c0 + i < cpw && kc < KC) load_chunk<FMT>(Wd, nullptr, H, I, rt, kc, lane, cd[i]);
             }
             if (c0 == 0) {
                 // split each fp32 activation into two 16-bit parts, hi + lo;
@@ -419,7 +440,6 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
         }
         __syncthreads();
     }
-    note_miss_end(s, d);
     // the CTA that finishes this row tile last combines it for every token
     __threadfence();
     __syncthreads();
@@ -450,6 +470,184 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
             }
             *s.tiles_done = 0u;
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Down projection of a decode call, one CTA per 16-row tile of the output
+// over every unit of the call. The unit descriptors and every pair's
+// activation (split into hi + lo 16-bit parts) are staged in shared memory
+// once; warps take (unit, group of kDRChunks chunks) items with all their
+// weight loads in flight; each item's partial tile goes to shared memory per
+// (chunk group, pair, row), and the CTA sums the groups in order, weights the
+// picks in rank order and adds the shared expert. No partial leaves the SM.
+// ---------------------------------------------------------------------------
+constexpr int kDRWarps = 16;
+constexpr int kDRChunks = 4;
+
+__host__ __device__ inline size_t down_rows_smem(int I, int KC, int U, int P) {
+    const size_t ld = (size_t)I + 8;
+    const int ncg = (KC + kDRChunks - 1) / kDRChunks;
+    return (size_t)U * sizeof(UnitDesc) + 2 * (size_t)(P + 1) * ld * 2 + (size_t)ncg * P * 16 * 4;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kDRWarps * 32, 1) k_down_rows(CacheDev c, Scratch s, float* __restrict__ out,
+                                                                 int T, int U, int bucket) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int IB = FMT == FMT_BF16 ? 1 : 2;  // items a warp keeps in flight
+    griddep_wait();
+    griddep_launch();
+    const int H = c.H, I = c.I, KC = I / 64, rt = blockIdx.x, k = c.k;
+    const int n_units = s.plan->n_units;
+    const int P = T * k + (c.has_shared ? T : 0);
+    const int ld = I + 8;
+    const int ncg = (KC + kDRChunks - 1) / kDRChunks;
+    UnitDesc* sd = reinterpret_cast<UnitDesc*>(smem);
+    uint16_t* ah = reinterpret_cast<uint16_t*>(smem + (size_t)U * sizeof(UnitDesc));
+    uint16_t* al = ah + (size_t)(P + 1) * ld;
+    float* ps = reinterpret_cast<float*>(al + (size_t)(P + 1) * ld);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    // stage the descriptors (uint4 words) and the activations (float4 -> hi/lo)
+    {
+        const int nw = n_units * (int)(sizeof(UnitDesc) / 16);
+        const uint4* src = reinterpret_cast<const uint4*>(s.units);
+        uint4* dst = reinterpret_cast<uint4*>(sd);
+        const int vpr = I / 4;
+        const int nv = P * vpr;
+        constexpr int B = 4;
+        for (int base = tid; base < nw + nv; base += nthr * B) {
+            float4 v[B];
+            uint4 w[B];
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+                const int j = base + i * nthr;
+                if (j < nw) w[i] = __ldcg(src + j);
+                else if (j < nw + nv) v[i] = __ldcg(reinterpret_cast<const float4*>(s.act) + (j - nw));
+            }
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+                const int j = base + i * nthr;
+                if (j < nw) {
+                    dst[j] = w[i];
+                } else if (j < nw + nv) {
+                    const int pr = (j - nw) / vpr, cv = (j - nw) - pr * vpr;
+                    const float av[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                    uint16_t hv[4], lv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (FMT == FMT_BF16) {
+                            __nv_bfloat16 h = __float2bfloat16_rn(av[q]);
+                            __nv_bfloat16 l = __float2bfloat16_rn(av[q] - __bfloat162float(h));
+                            hv[q] = *reinterpret_cast<uint16_t*>(&h);
+                            lv[q] = *reinterpret_cast<uint16_t*>(&l);
+                        } else {
+                            __half h = __float2half_rn(av[q]);
+                            __half l = __float2half_rn(av[q] - __half2float(h));
+                            hv[q] = *reinterpret_cast<uint16_t*>(&h);
+                            lv[q] = *reinterpret_cast<uint16_t*>(&l);
+                        }
+                    }
+                    *reinterpret_cast<uint2*>(ah + (size_t)pr * ld + cv * 4) =
+                        make_uint2(hv[0] | ((uint32_t)hv[1] << 16), hv[2] | ((uint32_t)hv[3] << 16));
+                    *reinterpret_cast<uint2*>(al + (size_t)pr * ld + cv * 4) =
+                        make_uint2(lv[0] | ((uint32_t)lv[1] << 16), lv[2] | ((uint32_t)lv[3] << 16));
+                }
+            }
+        }
+        for (int i = tid; i < ld / 2; i += nthr) {  // the zero row used for padding columns
+            reinterpret_cast<uint32_t*>(ah + (size_t)P * ld)[i] = 0u;
+            reinterpret_cast<uint32_t*>(al + (size_t)P * ld)[i] = 0u;
+        }
+    }
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+    const int n_items = n_units * ncg;
+    for (int it0 = warp * IB; it0 < n_items; it0 += kDRWarps * IB) {
+        Chunk<FMT> ch[IB][kDRChunks];
+#pragma unroll
+        for (int b = 0; b < IB; ++b) {
+            const int it = it0 + b;
+            if (it >= n_items) break;
+            const UnitDesc& d = sd[it / ncg];
+            const int cg = it - (it / ncg) * ncg;
+            const uint8_t* W = reinterpret_cast<const uint8_t*>(d.dst ? d.dst : d.src) + 2 * matrix_stride(FMT, I, H);
+#pragma unroll
+            for (int i = 0; i < kDRChunks; ++i) {
+                const int kc = cg * kDRChunks + i;
+                if (kc < KC) load_chunk<FMT>(W, nullptr, H, I, rt, kc, lane, ch[b][i]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < IB; ++b) {
+            const int it = it0 + b;
+            if (it >= n_items) break;
+            const UnitDesc& d = sd[it / ncg];
+            const int cg = it - (it / ncg) * ncg;
+            for (int n0 = 0; n0 < d.np; n0 += 8) {
+                // this lane's ldmatrix row: token column (lane & 7) of the tile
+                const int col = lane & 7;
+                const int pr = n0 + col < d.np ? (n0 + col < 8 ? d.pair8[n0 + col] : s.unit_pairs[d.pstart + n0 + col]) : P;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < kDRChunks; ++i) {
+                    const int kc = cg * kDRChunks + i;
+                    if (kc >= KC) break;
+                    if (n0 > 0) load_chunk<FMT>(reinterpret_cast<const uint8_t*>(d.dst ? d.dst : d.src) +
+                                                    2 * matrix_stride(FMT, I, H), nullptr, H, I, rt, kc, lane, ch[b][i]);
+                    uint32_t bf[2][4][2];
+                    const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                    const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                    ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
+                    ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
+                    ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
+                    ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
+                    mma_chunk<FMT, 2>(ch[b][i], bf, acc);
+                }
+                const float gd = d.g[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int cc = 2 * q + c2;
+                        if (n0 + cc < d.np) {
+                            const int pair = n0 + cc < 8 ? d.pair8[n0 + cc] : s.unit_pairs[d.pstart + n0 + cc];
+                            ps[((size_t)cg * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < T * 16; i += nthr) {
+        const int t = i >> 4, row = i & 15;
+        float y = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int pair = t * k + j;
+            float v = 0.f;
+            for (int cg = 0; cg < ncg; ++cg) v += ps[((size_t)cg * P + pair) * 16 + row];
+            y = fmaf(s.wts[pair], v, y);
+        }
+        if (c.has_shared) {
+            const int pair = T * k + t;
+            float v = 0.f;
+            for (int cg = 0; cg < ncg; ++cg) v += ps[((size_t)cg * P + pair) * 16 + row];
+            y += v;
+        }
+        out[(size_t)t * H + (size_t)rt * 16 + row] = y;
+    }
+    if (tid == 0 && atomicAdd(s.tiles_done, 1u) == gridDim.x - 1) {
+        // the last tile of the call books the time misses were streamed
+        __threadfence();
+        const unsigned long long t1 = atomicAdd(s.copy_t1, 0ull);
+        if (t1) {
+            const unsigned long long t0 = atomicAdd(s.copy_t0, 0ull);
+            c.stats[bucket * 5 + 4] += t1 - t0;
+            *s.copy_t0 = ~0ull;
+            *s.copy_t1 = 0ull;
+        }
+        *s.tiles_done = 0u;
     }
 }
 
@@ -544,6 +742,34 @@ static void down_fmt(const CacheDev& c, const Scratch& s, float* out, int T, int
     }
     dim3 grid(c.H / 16, units);
     launch_ex(k_down<FMT>, grid, dim3(kDNWarps * 32), sm, st, pdl, c, s, out, T, kind, group, G, bucket);
+}
+
+template <int FMT>
+static bool down_rows_fmt(const CacheDev& c, const Scratch& s, float* out, int T, int units, int bucket,
+                          cudaStream_t st, bool pdl) {
+    const int P = T * c.k + (c.has_shared ? T : 0);
+    const size_t sm = down_rows_smem(c.I, c.I / 64, units, P);
+    if (sm > 200 * 1024) return false;
+    static size_t set = 0;
+    if (sm > set) {
+        cudaFuncSetAttribute(k_down_rows<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        set = 200 * 1024;
+    }
+    launch_ex(k_down_rows<FMT>, dim3(c.H / 16), dim3(kDRWarps * 32), sm, st, pdl, c, s, out, T, units, bucket);
+    return true;
+}
+
+// Decode down projection: the row-tile kernel when its staging fits in
+// shared memory, else the per-unit kernel with a global combine.
+bool launch_down_rows(const CacheDev& c, const Scratch& s, float* out, int T, int units, int bucket, cudaStream_t st,
+                      bool pdl) {
+    switch (c.fmt) {
+    case FMT_BF16: return down_rows_fmt<FMT_BF16>(c, s, out, T, units, bucket, st, pdl);
+    case FMT_Q4_0: return down_rows_fmt<FMT_Q4_0>(c, s, out, T, units, bucket, st, pdl);
+    case FMT_FP8_B128: return down_rows_fmt<FMT_FP8_B128>(c, s, out, T, units, bucket, st, pdl);
+    case FMT_NVFP4: return down_rows_fmt<FMT_NVFP4>(c, s, out, T, units, bucket, st, pdl);
+    }
+    return false;
 }
 
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,

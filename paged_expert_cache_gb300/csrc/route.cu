@@ -42,17 +42,40 @@ __device__ __forceinline__ float2 norm_pair(float a, float b) {
     return make_float2(s, e);
 }
 
+// Copies n elements global -> shared with every thread's loads of a batch
+// in flight before its stores, so the copy costs one round trip per batch
+// instead of one per element.
+template <typename T, int B = 8>
+__device__ __forceinline__ void stage(T* dst, const T* src, int n, int tid, int nthr) {
+    for (int base = tid; base < n; base += nthr * B) {
+        T v[B];
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            if (base + i * nthr < n) v[i] = __ldcg(src + base + i * nthr);
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            if (base + i * nthr < n) dst[base + i * nthr] = v[i];
+    }
+}
+
+// Order-preserving map of a float to an unsigned integer.
+__device__ __forceinline__ unsigned ord32(float f) {
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Exact comparison of normalized pairs.
 __device__ __forceinline__ bool pair_gt(float2 a, float2 b) { return a.x > b.x || (a.x == b.x && a.y > b.y); }
 __device__ __forceinline__ bool pair_eq(float2 a, float2 b) { return a.x == b.x && a.y == b.y; }
 
-// Logits of one CTA's experts for one CTA's tokens, with their bounds.
+// Logits of one CTA's experts for one CTA's NT tokens, with their bounds.
+template <int NT>
 __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_t* smem, float2* logits,
                                    float* bounds) {
     const int H = c.H, E = c.E;
-    const int t0 = blockIdx.y * kRouteTokens;
-    const int nt = min(kRouteTokens, a.T - t0);
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [kRouteTokens][H]
+    const int t0 = blockIdx.y * NT;
+    const int nt = min(NT, a.T - t0);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [NT][H]
     const int vec_per_row = H / 8;
     for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
         int tt = i / vec_per_row, cv = i - tt * vec_per_row;
@@ -63,9 +86,9 @@ __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRouteWarps + warp;
     if (e >= E) return;
-    float hi[kRouteTokens], lo[kRouteTokens], ab[kRouteTokens];
+    float hi[NT], lo[NT], ab[NT];
 #pragma unroll
-    for (int tt = 0; tt < kRouteTokens; ++tt) hi[tt] = lo[tt] = ab[tt] = 0.f;
+    for (int tt = 0; tt < NT; ++tt) hi[tt] = lo[tt] = ab[tt] = 0.f;
     const uint16_t* wr = a.w + (size_t)e * H;
     constexpr int kMaxVec = 16;  // H <= 4096: all of a lane's weight vectors in flight at once
     const int nvec = H / 256;
@@ -80,8 +103,8 @@ __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_
         float wf[8] = {bf16_lo(wv[i].x), bf16_hi(wv[i].x), bf16_lo(wv[i].y), bf16_hi(wv[i].y),
                        bf16_lo(wv[i].z), bf16_hi(wv[i].z), bf16_lo(wv[i].w), bf16_hi(wv[i].w)};
 #pragma unroll
-        for (int tt = 0; tt < kRouteTokens; ++tt) {
-            if (tt < nt) {
+        for (int tt = 0; tt < NT; ++tt) {
+            if (NT == 1 || tt < nt) {
                 uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)tt * H + cb);
                 float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                                bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
@@ -101,7 +124,7 @@ __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
 #pragma unroll
-        for (int tt = 0; tt < kRouteTokens; ++tt) {
+        for (int tt = 0; tt < NT; ++tt) {
             float oh = __shfl_xor_sync(0xffffffffu, hi[tt], off);
             float ol = __shfl_xor_sync(0xffffffffu, lo[tt], off);
             float oa = __shfl_xor_sync(0xffffffffu, ab[tt], off);
@@ -123,7 +146,7 @@ __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_
         const float g = n * 0x1p-24f / (1.0f - n * 0x1p-24f);
         float hv = hi[0], lv = lo[0], av = ab[0];
 #pragma unroll
-        for (int tt = 1; tt < kRouteTokens; ++tt)
+        for (int tt = 1; tt < NT; ++tt)
             if (lane == tt) { hv = hi[tt]; lv = lo[tt]; av = ab[tt]; }
         float2 z = norm_pair(hv, lv);
         if (a.bias) {
@@ -166,24 +189,34 @@ __device__ __forceinline__ float2 shfl_pair(float2 v, int off) {
     return make_float2(__shfl_xor_sync(0xffffffffu, v.x, off), __shfl_xor_sync(0xffffffffu, v.y, off));
 }
 
-// Per-warp shared memory of the ranking: E entries of each array.
+// Per-warp shared memory of the ranking: E entries of each array plus the
+// k picks. The rounds below are rolled loops over these arrays: the kernel
+// runs this code once per call, so a short instruction stream matters more
+// than register-resident picks.
 struct TopkSmem {
     float2* z;    // logit pairs
     float* b;     // bounds
     int* cand;    // re-rank candidates
     double* z64;  // exact logits of the candidates
+    int* sel;     // [kMaxTopK] picks in rank order
+    float2* selz; // [kMaxTopK] their logit pairs
+    float* selb;  // [kMaxTopK] their bounds
 };
 
 __host__ __device__ inline size_t topk_bytes_per_warp(int E) {
-    return (size_t)E * (sizeof(float2) + sizeof(float) + sizeof(int) + sizeof(double));
+    return (size_t)E * (sizeof(float2) + sizeof(float) + sizeof(int) + sizeof(double)) +
+           (size_t)kMaxTopK * (sizeof(int) + sizeof(float2) + sizeof(float));
 }
 
 __device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
     TopkSmem t;
     t.z64 = reinterpret_cast<double*>(base);
     t.z = reinterpret_cast<float2*>(base + (size_t)E * 8);
-    t.b = reinterpret_cast<float*>(base + (size_t)E * 16);
-    t.cand = reinterpret_cast<int*>(base + (size_t)E * 20);
+    t.selz = reinterpret_cast<float2*>(base + (size_t)E * 16);
+    t.b = reinterpret_cast<float*>(base + (size_t)E * 16 + kMaxTopK * 8);
+    t.cand = reinterpret_cast<int*>(base + (size_t)E * 20 + kMaxTopK * 8);
+    t.sel = reinterpret_cast<int*>(base + (size_t)E * 24 + kMaxTopK * 8);
+    t.selb = reinterpret_cast<float*>(base + (size_t)E * 24 + kMaxTopK * 12);
     return t;
 }
 
@@ -191,34 +224,25 @@ __device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
 __device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
                            int* rerank_flag) {
     const int E = c.E, k = c.k, lane = threadIdx.x & 31;
-    for (int e = lane; e < E; e += 32) {
-        w.z[e] = __ldcg(s.logits + (size_t)t * E + e);
-        w.b[e] = __ldcg(s.bounds + (size_t)t * E + e);
-    }
+    stage<float2>(w.z, s.logits + (size_t)t * E, E, lane, 32);
+    stage<float>(w.b, s.bounds + (size_t)t * E, E, lane, 32);
     __syncwarp();
     // k rounds of argmax over the untaken experts; bit m of `taken` is e = lane + 32 m
     unsigned taken = 0;
-    int sel[kMaxTopK];
-    float2 selz[kMaxTopK];
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        float2 bz = make_float2(-INFINITY, 0.f);
+        int be = 0x7fffffff;
+        for (int e = lane, m = 0; e < E; e += 32, ++m)
+            if (!((taken >> m) & 1u) && better_pair(w.z[e], e, bz, be)) { bz = w.z[e]; be = e; }
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        sel[j] = 0;
-        selz[j] = make_float2(0.f, 0.f);
-        if (j < k) {
-            float2 bz = make_float2(-INFINITY, 0.f);
-            int be = 0x7fffffff;
-            for (int e = lane, m = 0; e < E; e += 32, ++m)
-                if (!((taken >> m) & 1u) && better_pair(w.z[e], e, bz, be)) { bz = w.z[e]; be = e; }
-#pragma unroll
-            for (int off = 16; off; off >>= 1) {
-                float2 oz = shfl_pair(bz, off);
-                int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (better_pair(oz, oe, bz, be)) { bz = oz; be = oe; }
-            }
-            sel[j] = be;
-            selz[j] = bz;
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        for (int off = 16; off; off >>= 1) {
+            float2 oz = shfl_pair(bz, off);
+            int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (better_pair(oz, oe, bz, be)) { bz = oz; be = oe; }
         }
+        if (lane == 0) { w.sel[j] = be; w.selz[j] = bz; }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
     }
     // largest upper bound (z + b, as a pair) over the experts not picked
     float2 mx = make_float2(-INFINITY, 0.f);
@@ -232,19 +256,19 @@ __device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs&
         float2 o = shfl_pair(mx, off);
         if (pair_gt(o, mx)) mx = o;
     }
+    __syncwarp();
     // certify: each pick's lower bound is above every later upper bound
     bool ok = true;
     float2 run = mx, lam = make_float2(INFINITY, 0.f);
-#pragma unroll
-    for (int jj = kMaxTopK - 1; jj >= 0; --jj) {
-        if (jj < k) {
-            const float bj = w.b[sel[jj]];
-            const float2 lower = norm_pair(selz[jj].x, __fsub_rd(selz[jj].y, bj));
-            const float2 upper = norm_pair(selz[jj].x, __fadd_ru(selz[jj].y, bj));
-            if (!pair_gt(lower, run)) ok = false;
-            if (pair_gt(upper, run)) run = upper;
-            if (pair_gt(lam, lower)) lam = lower;
-        }
+#pragma unroll 1
+    for (int j = k - 1; j >= 0; --j) {
+        const float2 zj = w.selz[j];
+        const float bj = w.b[w.sel[j]];
+        const float2 lower = norm_pair(zj.x, __fsub_rd(zj.y, bj));
+        const float2 upper = norm_pair(zj.x, __fadd_ru(zj.y, bj));
+        if (!pair_gt(lower, run)) ok = false;
+        if (pair_gt(upper, run)) run = upper;
+        if (pair_gt(lam, lower)) lam = lower;
     }
     if (!ok) {
         // candidates: every expert whose upper bound reaches the lowest lower
@@ -266,58 +290,178 @@ __device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs&
         __syncwarp();
         // k rounds over the candidates; a picked candidate is marked by
         // storing -1 - e in its cand entry
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k) {
-                double bz = -INFINITY;
-                int be = 0x7fffffff, bi = -1;
-                for (int i = lane; i < nc; i += 32) {
-                    int e = w.cand[i];
-                    if (e >= 0 && better(w.z64[i], e, bz, be)) { bz = w.z64[i]; be = e; bi = i; }
-                }
-#pragma unroll
-                for (int off = 16; off; off >>= 1) {
-                    double oz = __shfl_xor_sync(0xffffffffu, bz, off);
-                    int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                    int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (better(oz, oe, bz, be)) { bz = oz; be = oe; bi = oi; }
-                }
-                sel[j] = be;
-                selz[j] = w.z[be];
-                if (lane == (bi & 31)) w.cand[bi] = -1 - be;
-                __syncwarp();
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            double bz = -INFINITY;
+            int be = 0x7fffffff, bi = -1;
+            for (int i = lane; i < nc; i += 32) {
+                int e = w.cand[i];
+                if (e >= 0 && better(w.z64[i], e, bz, be)) { bz = w.z64[i]; be = e; bi = i; }
             }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                double oz = __shfl_xor_sync(0xffffffffu, bz, off);
+                int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (better(oz, oe, bz, be)) { bz = oz; be = oe; bi = oi; }
+            }
+            if (lane == 0) { w.sel[j] = be; w.selz[j] = w.z[be]; }
+            if (lane == (bi & 31)) w.cand[bi] = -1 - be;
+            __syncwarp();
         }
         if (lane == 0) *rerank_flag = 1;
     }
+    __syncwarp();
     // combine weights in fp32 from the picks' logits
-    float sum = 0.f;
-    float zref = selz[0].x;
+    float zref = -INFINITY, sum = 0.f;
     if (!c.norm_topk) {
-        float zmax = -INFINITY;
-        for (int e = lane; e < E; e += 32) zmax = fmaxf(zmax, w.z[e].x);
+        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
 #pragma unroll
-        for (int off = 16; off; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
-        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zmax);
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
 #pragma unroll
         for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        zref = zmax;
     } else {
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) zref = fmaxf(zref, selz[j].x);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) sum += expf(selz[j].x - zref);
+        for (int j = 0; j < k; ++j) zref = fmaxf(zref, w.selz[j].x);
+        for (int j = 0; j < k; ++j) sum += expf(w.selz[j].x - zref);
     }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < k && lane == (j & 31)) {
-            s.ids[t * k + j] = sel[j];
-            s.wts[t * k + j] = expf(selz[j].x - zref) / sum;
-        }
+    if (lane < k) {
+        s.ids[t * k + lane] = w.sel[lane];
+        s.wts[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
     }
     __syncwarp();
+}
+
+// Register-resident top-k: lane l holds the logits of experts l, l+32, ...
+// (NPL of them). A round is one warp argmax; only the lane whose expert was
+// taken rescans its registers. When the bounds do not separate the picks,
+// the token is ranked again by topk_token above (which re-ranks exactly).
+template <int NPL>
+__device__ void topk_token_reg(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
+                               int* rerank_flag) {
+    const int E = c.E, k = c.k, lane = threadIdx.x & 31;
+    float2 z[NPL];
+    float b[NPL];
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E) {
+            z[m] = __ldcg(s.logits + (size_t)t * E + e);
+            b[m] = __ldcg(s.bounds + (size_t)t * E + e);
+        } else {
+            z[m] = make_float2(-INFINITY, 0.f);
+            b[m] = 0.f;
+        }
+    }
+    // Rounds on integer keys: ord(hi), then ord(lo), then the lower expert id.
+    // ord() maps floats to unsigned integers in the same order; lo is
+    // normalised so -0 and +0 compare equal. The warp argmax is three
+    // single-instruction reductions.
+    unsigned kh[NPL], kl[NPL];
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+        const bool valid = lane + 32 * m < E;
+        kh[m] = valid ? ord32(z[m].x) : 0u;
+        kl[m] = valid ? ord32(__fadd_rn(z[m].y, 0.0f)) : 0u;
+    }
+    unsigned taken = 0, bh, bl, be;
+    int bm;
+    auto local_best = [&]() {
+        bh = 0u;
+        bl = 0u;
+        be = 0xffffffffu;
+        bm = -1;
+#pragma unroll
+        for (int m = 0; m < NPL; ++m) {
+            if (((taken >> m) & 1u) || kh[m] == 0u) continue;  // taken, or past E
+            if (kh[m] > bh || (kh[m] == bh && (kl[m] > bl || (kl[m] == bl && bm < 0)))) {
+                bh = kh[m];
+                bl = kl[m];
+                be = lane + 32 * m;
+                bm = m;
+            }
+        }
+        if (bh == 0u) be = 0xffffffffu;
+    };
+    local_best();
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        const unsigned uh = __reduce_max_sync(0xffffffffu, bh);
+        const unsigned ul = __reduce_max_sync(0xffffffffu, bh == uh ? bl : 0u);
+        const unsigned ue = __reduce_min_sync(0xffffffffu, (bh == uh && bl == ul) ? be : 0xffffffffu);
+        if ((int)(ue & 31) == lane) {
+            w.sel[j] = (int)ue;
+            w.selz[j] = z[bm];
+            w.selb[j] = b[bm];
+            taken |= 1u << bm;
+            local_best();
+        }
+    }
+    // largest upper bound over the experts not picked
+    float2 mx = make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E && !((taken >> m) & 1u)) {
+            float2 up = norm_pair(z[m].x, __fadd_ru(z[m].y, b[m]));
+            if (pair_gt(up, mx)) mx = up;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        float2 o = shfl_pair(mx, off);
+        if (pair_gt(o, mx)) mx = o;
+    }
+    __syncwarp();
+    bool ok = true;
+    float2 run = mx;
+#pragma unroll 1
+    for (int j = k - 1; j >= 0; --j) {
+        const float2 zj = w.selz[j];
+        const float bj = w.selb[j];
+        const float2 lower = norm_pair(zj.x, __fsub_rd(zj.y, bj));
+        const float2 upper = norm_pair(zj.x, __fadd_ru(zj.y, bj));
+        if (!pair_gt(lower, run)) ok = false;
+        if (pair_gt(upper, run)) run = upper;
+    }
+    if (!ok) {
+        topk_token(c, s, a, t, w, rerank_flag);
+        return;
+    }
+    float zref = -INFINITY, sum = 0.f;
+    if (!c.norm_topk) {
+#pragma unroll
+        for (int m = 0; m < NPL; ++m) zref = fmaxf(zref, z[m].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+#pragma unroll
+        for (int m = 0; m < NPL; ++m)
+            if (lane + 32 * m < E) sum += expf(z[m].x - zref);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    } else {
+        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
+        zref = zj;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        sum = lane < k ? expf(zj - zref) : 0.f;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
+    if (lane < k) {
+        s.ids[t * k + lane] = w.sel[lane];
+        s.wts[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void topk_dispatch(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
+                                              const TopkSmem& w, int* rerank_flag) {
+    if (c.E <= 32) topk_token_reg<1>(c, s, a, t, w, rerank_flag);
+    else if (c.E <= 128) topk_token_reg<4>(c, s, a, t, w, rerank_flag);
+    else if (c.E <= 256) topk_token_reg<8>(c, s, a, t, w, rerank_flag);
+    else if (c.E <= 512) topk_token_reg<16>(c, s, a, t, w, rerank_flag);
+    else topk_token(c, s, a, t, w, rerank_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -342,6 +486,7 @@ struct PlanSmem {
     unsigned long long* wmin;  // [32]
     int* wslot;              // [32]
     int* scal;               // [8]
+    float* gl;               // [(E+1)*3] NVFP4 global scales of the layer (+ shared)
     size_t bytes;
 };
 
@@ -370,6 +515,7 @@ __host__ __device__ inline PlanSmem plan_layout(uint8_t* base, int E, int K, int
     m.wmin = (unsigned long long*)take(sizeof(unsigned long long) * 32);
     m.wslot = (int*)take(sizeof(int) * 32);
     m.scal = (int*)take(sizeof(int) * 8);
+    m.gl = (float*)take(sizeof(float) * (E + 1) * 3);
     m.bytes = off;
     return m;
 }
@@ -395,19 +541,23 @@ __device__ void write_trace(const CacheDev& c, const Scratch& s, int layer, int 
     *c.trace_count = idx + 1;
 }
 
-__device__ void plan_prefetch(const CacheDev& c, const RouteArgs& a, const PlanSmem& m, int pool) {
+// Copies the pool's state into shared memory; run by threads tid of nthr
+// (the warps that are not ranking tokens, when there are any).
+__device__ void plan_prefetch(const CacheDev& c, const RouteArgs& a, const PlanSmem& m, int pool, int tid, int nthr,
+                              unsigned long long* clk) {
     const unsigned long long* lu = c.last_use + (size_t)pool * c.K;
     const int* kof = c.key_of + (size_t)pool * c.K;
     const int* smap = c.slot_map + (size_t)a.layer * c.E;
-    for (int i = threadIdx.x; i < c.K; i += blockDim.x) {
-        m.lu[i] = lu[i];
-        m.kof[i] = kof[i];
+    if (tid == 0) *clk = c.clock[pool];
+    stage<unsigned long long>(m.lu, lu, c.K, tid, nthr);
+    stage<int>(m.kof, kof, c.K, tid, nthr);
+    stage<int>(m.smap, smap, c.E, tid, nthr);
+    for (int e = tid; e < c.E; e += nthr) m.first[e] = 0x7fffffff;
+    if (c.fmt == FMT_NVFP4) {
+        stage<float>(m.gl, c.gtable + (size_t)a.layer * c.E * 3, c.E * 3, tid, nthr);
+        if (tid < 3) m.gl[c.E * 3 + tid] = c.gtable[((size_t)c.L * c.E + a.layer) * 3 + tid];
     }
-    for (int e = threadIdx.x; e < c.E; e += blockDim.x) {
-        m.smap[e] = smap[e];
-        m.first[e] = 0x7fffffff;
-    }
-    for (int i = threadIdx.x; i <= c.E / 32; i += blockDim.x) m.missbits[i] = 0u;
+    for (int i = tid; i <= c.E / 32; i += nthr) m.missbits[i] = 0u;
 }
 
 __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs& a, const PlanSmem& m,
@@ -583,9 +733,8 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
         UnitDesc d;
         d.pstart = m.u_cnt[u];
         d.np = m.u_cnt[u + 1] - m.u_cnt[u];
+#pragma unroll
         for (int j = 0; j < 8; ++j) d.pair8[j] = -1;
-        for (int i = 0, got = 0; i < P && got < 8 && got < d.np; ++i)
-            if (m.p_unit[i] == u) d.pair8[got++] = i;
         if (u < nu) {
             const int e = m.u_expert[u];
             const int sl = m.u_slot[u];
@@ -600,16 +749,19 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
                 d.src = slot_addr;
                 d.dst = 0;
             }
-            for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)layer * E + e) * 3 + j];
+            for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[e * 3 + j] : 1.0f;
         } else {
             d.expert = -1;
             d.slot = -1;
             d.hit = 1;
             d.src = (uint64_t)(c.shared_w + (size_t)layer * c.slot_stride);
             d.dst = 0;
-            for (int j = 0; j < 3; ++j) d.g[j] = c.gtable[((size_t)c.L * E + layer) * 3 + j];
+            for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[E * 3 + j] : 1.0f;
         }
         s.units[u] = d;
+        // the first eight pairs, written straight to the descriptor
+        for (int i = 0, got = 0; i < P && got < 8 && got < d.np; ++i)
+            if (m.p_unit[i] == u) s.units[u].pair8[got++] = i;
     }
     for (int i = tid; i < n_ids; i += nthr) {
         int u = m.unit_of[m.ids[i]];
@@ -626,21 +778,22 @@ __device__ void plan_decode(const CacheDev& c, const Scratch& s, const RouteArgs
         pl->n_units = n_units;
         pl->status = 0;
         unsigned long long* st = c.stats + a.bucket * 5;
-        st[0] += 1;
-        st[1] += (unsigned long long)nh;
-        st[2] += (unsigned long long)nmiss;
-        st[3] += (unsigned long long)nmiss * c.slot_bytes;
+        atomicAdd(st + 0, 1ull);
+        atomicAdd(st + 1, (unsigned long long)nh);
+        atomicAdd(st + 2, (unsigned long long)nmiss);
+        atomicAdd(st + 3, (unsigned long long)nmiss * c.slot_bytes);
         if (c.trace) write_trace(c, s, layer, T, n_ids, nh, nmiss, nu);
     }
 }
 
 // Fused decode routing: all CTAs compute logits; the last CTA to finish
 // prefetches the pool's state, ranks every token and runs the plan.
-__global__ void __launch_bounds__(kRouteThreads) k_route(CacheDev c, Scratch s, RouteArgs a) {
+template <int NT>
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route(CacheDev c, Scratch s, RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     griddep_wait();
     griddep_launch();
-    router_logits_tile(c, a, smem, s.logits, s.bounds);
+    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds);
     if (a.prefill) return;
     __threadfence();
     __syncthreads();
@@ -660,13 +813,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CacheDev c, Scratch s, 
     const int P = n_ids + (c.has_shared ? T : 0);
     const int pool = c.pool_mode ? 0 : a.layer;
     PlanSmem m = plan_layout(smem, E, c.K, n_ids, U, P);
-    plan_prefetch(c, a, m, pool);  // overlaps the ranking below
-    if (threadIdx.x == 0) clk = c.clock[pool];
     const int warp = threadIdx.x >> 5;
     const int nwt = min(kRouteWarps, T);
     const TopkSmem tw = topk_layout(smem + m.bytes + (size_t)warp * topk_bytes_per_warp(E), E);
-    if (warp < nwt)
-        for (int t = warp; t < T; t += nwt) topk_token(c, s, a, t, tw, &rerank);
+    if (nwt < kRouteWarps) {
+        // the ranking warps start at once; the others stage the pool's state
+        if (warp >= nwt) plan_prefetch(c, a, m, pool, threadIdx.x - nwt * 32, blockDim.x - nwt * 32, &clk);
+        else
+            for (int t = warp; t < T; t += nwt) topk_dispatch(c, s, a, t, tw, &rerank);
+    } else {
+        plan_prefetch(c, a, m, pool, threadIdx.x, blockDim.x, &clk);
+        for (int t = warp; t < T; t += nwt) topk_dispatch(c, s, a, t, tw, &rerank);
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         *s.route_done = 0;
@@ -686,7 +844,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk(CacheDev c, Scratch s, R
     if (threadIdx.x == 0) rerank = 0;
     __syncthreads();
     const TopkSmem tw = topk_layout(smem + (size_t)warp * topk_bytes_per_warp(E), E);
-    if (t < a.T) topk_token(c, s, a, t, tw, &rerank);
+    if (t < a.T) topk_dispatch(c, s, a, t, tw, &rerank);
     __syncthreads();
     if (threadIdx.x == 0 && rerank) atomicAdd(c.stats + 15, 1ull);
 }
@@ -823,16 +981,24 @@ size_t route_smem_bytes(const CacheDev& c, int T) {
     return x > last ? x : last;
 }
 
-void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /*max_units*/, cudaStream_t st,
-                  bool pdl) {
-    dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (a.T + kRouteTokens - 1) / kRouteTokens);
-    size_t sm = a.prefill ? (size_t)kRouteTokens * c.H * sizeof(uint16_t) : route_smem_bytes(c, a.T);
+template <int NT>
+static void route_nt(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st, bool pdl) {
+    dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (a.T + NT - 1) / NT);
+    size_t sm = a.prefill ? (size_t)NT * c.H * sizeof(uint16_t) : route_smem_bytes(c, a.T);
     static size_t set_route = 0;
     if (sm > set_route) {
-        cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        cudaFuncSetAttribute(k_route<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         set_route = sm;
     }
-    launch_ex(k_route, grid, dim3(kRouteThreads), sm, st, pdl, c, s, a);
+    launch_ex(k_route<NT>, grid, dim3(kRouteThreads), sm, st, pdl, c, s, a);
+}
+
+void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /*max_units*/, cudaStream_t st,
+                  bool pdl) {
+    if (a.T <= 1) route_nt<1>(c, s, a, st, pdl);
+    else if (a.T <= 2) route_nt<2>(c, s, a, st, pdl);
+    else if (a.T <= 4) route_nt<4>(c, s, a, st, pdl);
+    else route_nt<kRouteTokens>(c, s, a, st, pdl);
 }
 
 void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st) {
