@@ -235,6 +235,32 @@ moe_status_t moe_cache_profile_enable(moe_cache_t* h, int32_t on);
 /* Synchronises, returns the totals since the last read and clears them. */
 moe_status_t moe_cache_profile_read(moe_cache_t* h, moe_profile_t* out);
 
+/* Router + top-k of one layer that allocates nothing (no counterpart on the
+ * pages: it exists for callers of this library that cannot call cudaMalloc
+ * where they route tokens -- code running inside CUDA graph capture, custom
+ * allocators that must not be re-entered from their own callbacks, embedders
+ * that budget all device memory up front). Computes, for T tokens, the same
+ * routing as moe_layer_forward: logits = hidden x router_w^T (+ bias), the
+ * top_k experts with ties to the lower id, and their weights (softmax over the
+ * picks when norm_topk, else the full softmax read at the picks).
+ *   hidden      : device bf16 [T x hidden_size]
+ *   router_w    : device bf16 [num_experts x hidden_size]
+ *   router_bias : device fp32 [num_experts] or NULL
+ *   ids         : device int32 [T x top_k] (output, rank order per token)
+ *   weights     : device fp32 [T x top_k] (output)
+ * Limits: T <= 32, num_experts <= 512, top_k <= 16, hidden_size a multiple of
+ * 64 up to 4096; anything else returns MOE_ERR_INVALID without launching.
+ * Scratch: a fixed 196,864-byte array inside the library, held by every GPU
+ * that loads it until the process exits; no call allocates or frees memory.
+ * The first call on a device looks up the array's device address (make that
+ * call before any stream capture); every later call only enqueues a memset of
+ * an internal counter and one kernel on `stream`. All calls on a device share
+ * the array, so calls whose kernels overlap on the GPU (unordered streams)
+ * race. Asynchronous; MOE_ERR_CUDA if a launch fails. */
+moe_status_t moe_route_topk_noalloc(const void* hidden, int32_t T, const void* router_w, const float* router_bias,
+                                    int32_t num_experts, int32_t hidden_size, int32_t top_k, int32_t norm_topk,
+                                    int32_t* ids, float* weights, void* stream);
+
 /* Synchronises, empties every slot, restores the initial LRU order and clears
  * the counters and trace. Expert data stays loaded. */
 moe_status_t moe_cache_reset(moe_cache_t* h);

@@ -88,6 +88,7 @@ def load():
         "moe_cache_read_slot": (i32, [vp, i32, i32, vp, i32, i32, vp, u64]),
         "moe_cache_profile_enable": (i32, [vp, i32]),
         "moe_cache_profile_read": (i32, [vp, P(MoeProfile)]),
+        "moe_route_topk_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
         "moe_cache_reset": (i32, [vp]),
         "moe_cache_destroy": (i32, [vp]),
     }
@@ -146,6 +147,24 @@ def _ptr(t):
     if isinstance(t, np.ndarray):
         return t.ctypes.data
     return t.data_ptr()
+
+
+def route_topk_noalloc(hidden, router_w, ids, weights, top_k, bias=None, norm_topk=True, stream=None):
+    """moe_route_topk_noalloc: routing of T tokens into caller-provided ids
+    [T, k] (int32) and weights [T, k] (fp32), with no allocation."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    if stream is None:
+        try:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        except Exception:
+            stream = 0
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check(load().moe_route_topk_noalloc(_ptr(hidden), T, _ptr(router_w), _ptr(bias), E, H, top_k,
+                                         1 if norm_topk else 0, _ptr(ids), _ptr(weights), stream or None))
+    return ids, weights
 
 
 class MoECache:

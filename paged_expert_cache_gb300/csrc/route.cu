@@ -18,6 +18,11 @@
 // bounds cannot separate the ranking are the candidates recomputed in the
 // definition's own order (sequential fp64, no fused multiply-add) and ranked
 // again.
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_cache.h"
 #include "common.cuh"
 
 namespace moe {
@@ -1022,3 +1027,133 @@ void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Router + top-k for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc where they route tokens: code running
+// while a CUDA graph is being captured (an allocation there breaks the
+// capture), allocators that must not be re-entered from their own callbacks,
+// and embedders that budget every byte of device memory up front. For them
+// moe_route_topk_noalloc computes one layer's routing (logits, top-k,
+// weights) without allocating: its scratch (the logit pairs, their bounds
+// and a completion counter) lives in the file-scope array below, which every
+// GPU that loads the library holds until the process exits. The array is
+// shared by every call on a device and keeps the last call's contents; the
+// counter is cleared at the start of each call. Calls whose kernels overlap
+// on one GPU race on the array.
+// ---------------------------------------------------------------------------
+namespace moe {
+
+constexpr int kNoAllocMaxTokens = 32;
+constexpr int kNoAllocMaxExperts = 512;
+constexpr size_t kNoAllocLogitBytes = (size_t)kNoAllocMaxTokens * kNoAllocMaxExperts * sizeof(float2);
+constexpr size_t kNoAllocBoundBytes = (size_t)kNoAllocMaxTokens * kNoAllocMaxExperts * sizeof(float);
+constexpr size_t kNoAllocScratchBytes = kNoAllocLogitBytes + kNoAllocBoundBytes + 256;
+
+// [logit pairs][bounds][completion counter]
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// All CTAs compute logits; the last one to finish ranks every token.
+template <int NT>
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route_noalloc(CacheDev c, Scratch s, RouteArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds);
+    __threadfence();
+    __syncthreads();
+    __shared__ int is_last;
+    __shared__ int rerank;
+    if (threadIdx.x == 0) {
+        is_last = atomicAdd(s.route_done, 1u) == gridDim.x * gridDim.y - 1;
+        rerank = 0;
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int warp = threadIdx.x >> 5;
+    const int nwt = min(kRouteWarps, a.T);
+    const TopkSmem tw = topk_layout(smem + (size_t)warp * topk_bytes_per_warp(c.E), c.E);
+    if (warp < nwt)
+        for (int t = warp; t < a.T; t += nwt) topk_dispatch(c, s, a, t, tw, &rerank);
+}
+
+template <int NT>
+static cudaError_t route_noalloc_nt(const CacheDev& c, const Scratch& s, const RouteArgs& a, size_t sm,
+                                    cudaStream_t st) {
+    dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (a.T + NT - 1) / NT);
+    cudaError_t e = cudaFuncSetAttribute(k_route_noalloc<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    k_route_noalloc<NT><<<grid, kRouteThreads, sm, st>>>(c, s, a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace {
+
+// Device address of g_noalloc_scratch, looked up once per device (the host
+// symbol is only a stand-in and must never be handed to a kernel).
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {nullptr};
+
+cudaError_t noalloc_scratch(int dev, unsigned char** out) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, moe::g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_route_topk_noalloc(const void* hidden, int32_t T, const void* router_w,
+                                               const float* router_bias, int32_t num_experts, int32_t hidden_size,
+                                               int32_t top_k, int32_t norm_topk, int32_t* ids, float* weights,
+                                               void* stream) {
+    if (!hidden || !router_w || !ids || !weights) return MOE_ERR_INVALID;
+    if (T < 1 || T > moe::kNoAllocMaxTokens || num_experts < 1 || num_experts > moe::kNoAllocMaxExperts ||
+        top_k < 1 || top_k > moe::kMaxTopK || top_k > num_experts || hidden_size < 64 || hidden_size % 64 ||
+        hidden_size > 4096)
+        return MOE_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    unsigned char* base = nullptr;
+    if (noalloc_scratch(dev, &base) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    moe::CacheDev c;
+    memset(&c, 0, sizeof c);
+    c.E = num_experts;
+    c.k = top_k;
+    c.H = hidden_size;
+    c.norm_topk = norm_topk ? 1 : 0;
+    moe::Scratch s;
+    memset(&s, 0, sizeof s);
+    s.logits = reinterpret_cast<float2*>(base);
+    s.bounds = reinterpret_cast<float*>(base + moe::kNoAllocLogitBytes);
+    s.route_done = reinterpret_cast<unsigned*>(base + moe::kNoAllocLogitBytes + moe::kNoAllocBoundBytes);
+    s.ids = ids;
+    s.wts = weights;
+    moe::RouteArgs a;
+    a.x = (const uint16_t*)hidden;
+    a.w = (const uint16_t*)router_w;
+    a.bias = router_bias;
+    a.T = T;
+    a.layer = 0;
+    a.prefill = 0;
+    a.bucket = 0;
+    if (cudaMemsetAsync(s.route_done, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t xs = (size_t)moe::kRouteTokens * hidden_size * sizeof(uint16_t);
+    const size_t tk = (size_t)min(moe::kRouteWarps, (int)T) * moe::topk_bytes_per_warp(num_experts);
+    const size_t sm = xs > tk ? xs : tk;
+    cudaError_t e;
+    if (T <= 1) e = moe::route_noalloc_nt<1>(c, s, a, sm, st);
+    else if (T <= 2) e = moe::route_noalloc_nt<2>(c, s, a, sm, st);
+    else if (T <= 4) e = moe::route_noalloc_nt<4>(c, s, a, sm, st);
+    else e = moe::route_noalloc_nt<moe::kRouteTokens>(c, s, a, sm, st);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,58 @@
+"""The routing entry point that allocates nothing (moe_route_topk_noalloc).
+
+It serves callers that cannot allocate device memory where they route
+tokens (for example code running under CUDA graph capture). Its ids must be
+exactly those moe_layer_forward routes the same tokens to, and its weights
+those of the oracle, on two calls in a row that share the library's fixed
+scratch array. Collected last so a failure here does not hide the others.
+"""
+import numpy as np
+import pytest
+
+from harness import OracleRun, Setup, cuda_available
+from synth.workloads import WORKLOADS, scaled
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.mark.parametrize("name,T", [("qwen3_30b_a3b_fp8", 4), ("flash_next_nvfp4", 1), ("tiny", 4)])
+def test_noalloc_routing_matches_the_layer_forward(name, T):
+    import torch
+    import paged_expert_cache_gb300 as pec
+    base = WORKLOADS[name]
+    w = scaled(base, L=1, H=min(base.H, 512), I=128, streams=(T,), steps=2,
+               slots_per_layer=max(base.slots_per_layer, T * base.k), pool_bytes=0.0, pool_mode="per_layer",
+               has_shared=False)
+    st = Setup(w, max_tokens=T)
+    orc = OracleRun(w, st.info["slot_bytes"])
+    xs = st.hiddens(0, T, 2)
+    ids = torch.empty((T, w.k), dtype=torch.int32, device=st.dev)
+    wts = torch.empty((T, w.k), dtype=torch.float32, device=st.dev)
+    for step in range(2):  # two calls in a row share the scratch array
+        st.forward(xs[step], 0)
+        rec = st.cache.trace_read()[0]
+        x = torch.from_numpy(np.ascontiguousarray(xs[step]).view(np.int16)).to(st.dev)
+        pec.route_topk_noalloc(x, st.router_dev[0], ids, wts, w.k, bias=st.bias_dev)
+        torch.cuda.synchronize()
+        got_ids = ids.cpu().numpy().reshape(-1)
+        assert np.array_equal(got_ids, rec["ids"]), (got_ids, rec["ids"])
+        want_ids, want_w = orc.route(xs[step], st.router[0], st.bias)
+        assert np.array_equal(got_ids, want_ids.reshape(-1))
+        assert np.allclose(wts.cpu().numpy(), want_w, rtol=1e-5, atol=1e-7)
+    st.close()
+
+
+def test_noalloc_refuses_sizes_beyond_its_scratch():
+    import torch
+    import paged_expert_cache_gb300 as pec
+    dev = torch.device("cuda:0")
+    x = torch.zeros((33, 256), dtype=torch.int16, device=dev)
+    wr = torch.zeros((16, 256), dtype=torch.int16, device=dev)
+    ids = torch.empty((33, 2), dtype=torch.int32, device=dev)
+    wts = torch.empty((33, 2), dtype=torch.float32, device=dev)
+    with pytest.raises(pec.MoeError) as ei:
+        pec.route_topk_noalloc(x, wr, ids, wts, 2)
+    assert ei.value.status == pec.ERR_INVALID
+    wr_big = torch.zeros((513, 256), dtype=torch.int16, device=dev)
+    with pytest.raises(pec.MoeError):
+        pec.route_topk_noalloc(x[:1], wr_big, ids[:1], wts[:1], 2)
