@@ -54,6 +54,24 @@ def matrix_bytes(fmt, R, C):
     return R * C // 2 + R * (C // 16)
 
 
+def replica_workload(w, rank):
+    """Independent replicas: every rank but 0 draws its own seeded streams."""
+    from synth.workloads import scaled
+    return scaled(w, index=w.index + 100 * rank) if rank else w
+
+
+def aggregate(ms, tokens, dist=None, device="cpu"):
+    """Whole-job figures of N independent replicas: (slowest rank's ms, tokens of all ranks)."""
+    if dist is None:
+        return ms, tokens
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -244,8 +262,7 @@ def run_ours(args):
     from synth.workloads import WORKLOADS, scaled
     w = WORKLOADS[args.workload]
     T = args.batch or w.streams[0]
-    if rank:  # independent replicas: each rank draws its own inputs
-        w = scaled(w, index=w.index + 100 * rank)
+    w = replica_workload(w, rank)
     if args.layers:
         w = scaled(w, L=args.layers)
     if args.slots:
@@ -326,17 +343,12 @@ def run_ours(args):
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, tokens = aggregate(ev0.elapsed_time(ev1), args.steps * T, dist, dev)
     s1 = cache.stats()
     b0, b1 = s0["buckets"][0], s1["buckets"][0]
     hits, misses = b1["hits"] - b0["hits"], b1["misses"] - b0["misses"]
     up_bytes = b1["bytes_uploaded"] - b0["bytes_uploaded"]
     up_ns = b1["upload_ns"] - b0["upload_ns"]
-    tokens = args.steps * T * world
     value = tokens / (ms / 1e3)
 
     # e2e: inputs from pinned host memory each step, outputs read back each step
@@ -355,11 +367,7 @@ def run_ours(args):
         h_out.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, _ = aggregate(e0.elapsed_time(e1), args.steps * T, dist, dev)
     cursor = PRIME + args.warmup + 2 * args.steps
 
     # Per-launch device time of every stage, call by call over further steps of
