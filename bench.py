@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU sample")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
+    ap.add_argument("--fused", action="store_true", help="one persistent kernel per decode call")
     return ap.parse_args()
 
 
@@ -270,7 +271,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
-                          max_tokens=max(T, 1), device=local)
+                          max_tokens=max(T, 1), device=local, split_decode=not args.fused)
     t_setup = time.perf_counter()
     cache = pec.MoECache(cfg)
     buf = None
@@ -389,7 +390,7 @@ def run_ours(args):
             prof = cache.profile_read()
             calls.append((cache.stats()["buckets"][0]["misses"] - m0, prof))
     cache.profile_enable(False)
-    stages = ("route", "copy", "gateup", "down")
+    stages = ("route", "copy", "gateup", "down", "layer")
     launches_per_call = sum(sum(p[k]["launches"] for k in stages) for _, p in calls) / len(calls)
 
     def mean_us(stage, sel):
@@ -410,13 +411,19 @@ def run_ours(args):
     gu_hit, n_hit_calls = mean_us("gateup", hit)
     dn_hit, _ = mean_us("down", hit)
     rt_hit, _ = mean_us("route", hit)
+    ly_hit, n_hit_layer = mean_us("layer", hit)
     gu_all, _ = mean_us("gateup", anyc)
     dn_all, _ = mean_us("down", anyc)
     rt_all, _ = mean_us("route", anyc)
+    ly_all, _ = mean_us("layer", anyc)
     gbs = lambda nbytes, us: nbytes / (us * 1e-6) / 1e9 if us else None
     gu_gbs = gbs(gu_bytes, gu_hit)
     dn_gbs = gbs(dn_bytes, dn_hit)
-    ffn_hit_us = (rt_hit or 0) + (gu_hit or 0) + (dn_hit or 0)
+    fused = ly_hit is not None
+    # one call's algorithmic bytes: router, tokens, every unit's record once,
+    # activations written and read back, the output
+    call_bytes = rt_bytes + units * rec_bytes + 2 * units * T * w.I * 4 + T * w.H * 4
+    ffn_hit_us = ly_hit if fused else (rt_hit or 0) + (gu_hit or 0) + (dn_hit or 0)
     ffn_gbs_hit = gbs(units * rec_bytes + rt_bytes, ffn_hit_us)
     tot = {k: sum(p[k]["ms"] for _, p in calls) for k in stages}
     dominant = max(stages, key=lambda k: tot[k])
@@ -447,11 +454,21 @@ def run_ours(args):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
-    roofline = {"bound": "hbm", "kernel": "k_gateup (gate/up + SwiGLU GEMV, resident-hit launches)",
-                "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None, "peak_src": peaks["src"] + " copy bandwidth",
-                "traffic": traffic, "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": gu_hit,
-                "launches_averaged": n_hit_calls, "dominant_stage": dominant}
+    if fused:
+        ly_gbs = gbs(call_bytes, ly_hit)
+        roofline = {"bound": "hbm", "kernel": "k_layer (whole decode call in one kernel, resident-hit launches)",
+                    "achieved": ly_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ly_gbs / peaks["hbm_gbs"] if ly_gbs else None,
+                    "peak_src": peaks["src"] + " copy bandwidth", "traffic": traffic,
+                    "algorithmic_bytes_per_launch": call_bytes, "avg_launch_us": ly_hit,
+                    "launches_averaged": n_hit_layer, "dominant_stage": dominant}
+    else:
+        roofline = {"bound": "hbm", "kernel": "k_gateup (gate/up + SwiGLU GEMV, resident-hit launches)",
+                    "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None,
+                    "peak_src": peaks["src"] + " copy bandwidth", "traffic": traffic,
+                    "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": gu_hit,
+                    "launches_averaged": n_hit_calls, "dominant_stage": dominant}
 
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
@@ -477,8 +494,9 @@ def run_ours(args):
                                else None, "frac_of_8tbs": ffn_gbs_hit / 8000.0 if ffn_gbs_hit else None,
                                "bytes_per_call": units * rec_bytes + rt_bytes, "us_per_call": ffn_hit_us},
         "kernel_gbs_all_hit": {"gateup": gu_gbs, "down": dn_gbs},
-        "stage_us_per_launch": {"all_hit": {"route": rt_hit, "gateup": gu_hit, "down": dn_hit},
-                                "all_calls": {"route": rt_all, "gateup": gu_all, "down": dn_all}},
+        "stage_us_per_launch": {"all_hit": {"route": rt_hit, "gateup": gu_hit, "down": dn_hit, "layer": ly_hit},
+                                "all_calls": {"route": rt_all, "gateup": gu_all, "down": dn_all, "layer": ly_all}},
+        "decode_path": "one kernel per layer call" if fused else "route, gate/up, down kernels",
         "stage_share": {k: tot[k] / sum(tot.values()) for k in stages},
         "profiled_calls": len(calls), "profiled_all_hit_calls": n_hit_calls, "profiled_misses": pmiss,
         "roofline": roofline,

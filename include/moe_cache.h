@@ -105,10 +105,15 @@ typedef struct {
     int32_t prefill_group;    /* experts staged per prefill group (32) */
     int32_t max_tokens;       /* largest T of any call (sizes scratch) */
     int32_t device;           /* CUDA device ordinal */
+    int32_t split_decode;     /* 0: a decode call that fits (T <= 8, T*k (+T shared) <= 48, PULL
+                                 uploads) runs as one persistent kernel, one CTA per SM with two
+                                 bounded grid barriers; 1 (default): always three kernels (route,
+                                 gate/up, down). Both give bitwise identical results. */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
- * max_tokens 32, upload PULL, per-layer pools; shape fields zero. */
+ * max_tokens 32, upload PULL, per-layer pools, split_decode 1; shape fields
+ * zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {
@@ -136,6 +141,8 @@ typedef struct {
     uint64_t pool_device_bytes;   /* slot pool(s) in HBM */
     uint64_t store_host_bytes;    /* pinned host store, every expert of every layer */
     uint64_t scratch_device_bytes;
+    uint64_t fused_decode_calls;  /* decode calls launched as one kernel (split_decode 0) */
+    uint64_t split_decode_calls;  /* decode calls launched as route, gate/up, down kernels */
 } moe_info_t;
 
 typedef struct moe_cache moe_cache_t;
@@ -189,7 +196,12 @@ moe_status_t moe_cache_load_shared(moe_cache_t* h, int32_t layer, const void* re
 moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, const void* router_w,
                                const float* router_bias, int32_t layer_id, float* out, void* stream);
 
-/* Synchronises the device and copies the counters out. */
+/* Synchronises the device and copies the counters out. Returns
+ * MOE_ERR_TIMEOUT (counters still copied) if a grid barrier of the one-kernel
+ * decode path gave up waiting since the last reset: every CTA of that kernel
+ * must be resident at once, which another workload holding SMs for over
+ * 0.2 s can prevent; the handle's state is then suspect until
+ * moe_cache_reset. */
 moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out);
 
 /* Sizes and layout facts of the handle (host only, no sync). */
@@ -223,8 +235,8 @@ moe_status_t moe_cache_read_slot(moe_cache_t* h, int32_t pool, int32_t slot, voi
  * forward launches is bracketed by CUDA events on the forward's stream (do
  * not enable it while capturing a CUDA graph). Stages: 0 router + top-k +
  * plan, 1 miss copies, 2 gate/up + SwiGLU, 3 down + combine, 4 prefill top-k,
- * 5 prefill plan. */
-#define MOE_NUM_STAGES 6
+ * 5 prefill plan, 6 the whole decode call in one kernel (split_decode 0). */
+#define MOE_NUM_STAGES 7
 typedef struct {
     double ms[MOE_NUM_STAGES];         /* summed event time per stage */
     uint64_t launches[MOE_NUM_STAGES]; /* kernels timed per stage */

@@ -30,7 +30,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("num_layers", i32), ("num_experts", i32), ("top_k", i32), ("hidden", i32), ("inter", i32),
                 ("format", i32), ("has_shared", i32), ("pool_mode", i32), ("slots_per_layer", i32),
                 ("upload_mode", i32), ("pool_bytes", dbl), ("norm_topk", i32), ("max_cache_tokens", i32),
-                ("prefill_group", i32), ("max_tokens", i32), ("device", i32)]
+                ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32)]
 
 
 class BucketStats(ctypes.Structure):
@@ -45,11 +45,11 @@ class MoeStats(ctypes.Structure):
 class MoeInfo(ctypes.Structure):
     _fields_ = [("num_pools", i32), ("slots_per_pool", i32), ("slot_bytes", u64), ("slot_stride", u64),
                 ("record_bytes", u64), ("pool_device_bytes", u64), ("store_host_bytes", u64),
-                ("scratch_device_bytes", u64)]
+                ("scratch_device_bytes", u64), ("fused_decode_calls", u64), ("split_decode_calls", u64)]
 
 
-NUM_STAGES = 6
-STAGES = ["route", "copy", "gateup", "down", "prefill_topk", "prefill_plan"]
+NUM_STAGES = 7
+STAGES = ["route", "copy", "gateup", "down", "prefill_topk", "prefill_plan", "layer"]
 
 
 class MoeProfile(ctypes.Structure):
@@ -121,7 +121,7 @@ def _check(st, handle=None):
 
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
-                max_tokens=32, device=0):
+                max_tokens=32, device=0, split_decode=True):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -136,6 +136,7 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.prefill_group = prefill_group
     c.max_tokens = max_tokens
     c.device = device
+    c.split_decode = 1 if split_decode else 0
     return c
 
 

@@ -35,6 +35,8 @@ struct moe_cache {
     std::vector<float> gtable_host;
     // per-stage event timing
     bool prof_on = false;
+    bool fused_ok = true;  // the one-kernel decode path launched (or was not tried yet)
+    uint64_t fused_calls = 0, split_calls = 0;
     std::vector<cudaEvent_t> ev_pool;
     size_t ev_used = 0;
     struct Span { int stage, a, b; };
@@ -113,6 +115,8 @@ moe_status_t init_tables(moe_cache_t* h) {
     CK(h, cudaMemcpy(d.last_use, lu.data(), lu.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.clock, clk.data(), clk.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
     CK(h, cudaMemset(d.stats, 0, 16 * sizeof(unsigned long long)));
+    if (h->scr.grid_bar) CK(h, cudaMemset(h->scr.grid_bar, 0, sizeof(unsigned)));
+    if (h->scr.err) CK(h, cudaMemset(h->scr.err, 0, sizeof(unsigned)));
     if (d.trace_count) CK(h, cudaMemset(d.trace_count, 0, sizeof(unsigned long long)));
     memset(h->memcpy_upload_ns, 0, sizeof(h->memcpy_upload_ns));
     return MOE_OK;
@@ -135,6 +139,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->prefill_group = 32;
     cfg->max_tokens = 32;
     cfg->device = 0;
+    cfg->split_decode = 1;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -275,12 +280,15 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.copy_t0, 1);
     DA(s.copy_t1, 1);
     DA(s.tiles_done, 1);
+    DA(s.grid_bar, 1);
+    DA(s.err, 1);
 #undef DA
     h->scratch_bytes = T * d.E * 16 + T * d.k * 16 + U * (sizeof(moe::UnitDesc) + 32) + P * 8 + P * (d.I + d.H) * 4;
     if (cudaMemset(s.route_done, 0, 4) != cudaSuccess || cudaMemset(s.tile_done, 0, (d.H / 16) * 4) != cudaSuccess ||
         cudaMemset(s.copy_done, 0, 4) != cudaSuccess || cudaMemset(s.copy_t0, 0xff, 8) != cudaSuccess ||
         cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess ||
-        cudaMemset(s.tiles_done, 0, 4) != cudaSuccess)
+        cudaMemset(s.tiles_done, 0, 4) != cudaSuccess || cudaMemset(s.grid_bar, 0, 4) != cudaSuccess ||
+        cudaMemset(s.err, 0, 4) != cudaSuccess)
         return bail(MOE_ERR_CUDA, "scratch initialisation failed");
     if (c.upload_mode == MOE_UPLOAD_MEMCPY) {
         e = cudaHostAlloc((void**)&h->host_fill, sizeof(int) * (2 + 2 * U), cudaHostAllocDefault);
@@ -383,10 +391,23 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     // programmatic dependent launch between the decode kernels (off while
     // events bracket each launch for profiling)
     const bool pdl = !h->prof_on;
-    if (decode) {
-        // PULL: misses are pulled over the host link by the expert kernels
-        // themselves (gate/up and down each stream their part of a missed
-        // record into its slot while they consume it)
+    bool fused = false;
+    if (decode && !h->cfg.split_decode && h->fused_ok && h->cfg.upload_mode == MOE_UPLOAD_PULL &&
+        moe::layer_smem_bytes(d, T) > 0) {
+        // the whole call in one persistent kernel
+        timed(h, 6, st, [&] { fused = moe::launch_layer(d, h->scr, a, out, bucket, st, pdl); });
+        if (!fused) {
+            // not launchable here (e.g. one CTA per SM does not fit): clear the
+            // launch error and keep to the three-kernel path from now on
+            cudaGetLastError();
+            h->fused_ok = false;
+            if (h->prof_on && !h->spans.empty()) h->spans.pop_back();
+        }
+    }
+    if (decode) ++(fused ? h->fused_calls : h->split_calls);
+    if (decode && !fused) {
+        // PULL: misses are pulled over the host link by the gate/up kernel,
+        // which streams each missed record into its slot while it consumes it
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, pdl); });
         if (h->cfg.upload_mode == MOE_UPLOAD_MEMCPY) {
             // read the fill list back, then one copy per merged run
@@ -421,7 +442,7 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
             if (!moe::launch_down_rows(d, h->scr, out, T, units, bucket, st, pdl))
                 moe::launch_down(d, h->scr, out, T, 0, 0, h->G, units, bucket, st, pdl);
         });
-    } else {
+    } else if (!decode) {
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, false); });
         timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });
         timed(h, 5, st, [&] { moe::launch_plan_prefill(d, h->scr, a, h->G, st); });
@@ -458,6 +479,9 @@ moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out) {
     out->slot_bytes = h->slot_bytes;
     out->record_bytes = h->record_bytes;
     out->topk_fp64_rerank = st[15];
+    unsigned derr = 0;
+    CK(h, cudaMemcpy(&derr, h->scr.err, sizeof derr, cudaMemcpyDeviceToHost));
+    if (derr & 1u) return fail(h, MOE_ERR_TIMEOUT, "a grid barrier of the one-kernel decode path timed out");
     return MOE_OK;
 }
 
@@ -471,6 +495,8 @@ moe_status_t moe_cache_info(moe_cache_t* h, moe_info_t* out) {
     out->pool_device_bytes = h->pool_bytes_dev;
     out->store_host_bytes = h->store_bytes;
     out->scratch_device_bytes = h->scratch_bytes;
+    out->fused_decode_calls = h->fused_calls;
+    out->split_decode_calls = h->split_calls;
     return MOE_OK;
 }
 

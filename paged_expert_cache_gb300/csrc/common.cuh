@@ -94,6 +94,8 @@ struct Scratch {
     unsigned long long* copy_t0;  // miss streaming start / end (globaltimer ns)
     unsigned long long* copy_t1;
     unsigned* tiles_done;   // row tiles combined by the down kernel (whole call)
+    unsigned* grid_bar;     // arrival counter of the fused layer kernel's grid barriers
+    unsigned* err;          // sticky device error bits (1: a grid barrier timed out)
 };
 
 // Device cache state and constants of a handle.
@@ -258,6 +260,12 @@ inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 size_t route_smem_bytes(const CacheDev& c, int T);
+// Fused decode layer: the dynamic shared memory a call of T tokens needs, or 0
+// when the call is outside the kernel's limits; and the launch (false when
+// the call does not fit, so the caller takes the three-kernel path).
+size_t layer_smem_bytes(const CacheDev& c, int T);
+bool launch_layer(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, int bucket, cudaStream_t st,
+                  bool pdl);
 bool launch_down_rows(const CacheDev& c, const Scratch& s, float* out, int T, int units, int bucket, cudaStream_t st,
                       bool pdl);
 

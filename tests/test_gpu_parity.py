@@ -197,3 +197,55 @@ def test_exact_ties_rank_the_lower_expert_first():
     run_steps(st, orc, 4, 3)
     assert st.cache.stats()["topk_fp64_rerank"] > 0
     st.close()
+
+
+@pytest.mark.parametrize("fmt,pool_mode,E,T", [
+    ("q4_0", "per_layer", 64, 1), ("q4_0", "shared", 64, 3), ("fp8_b128", "per_layer", 40, 8),
+    ("nvfp4", "shared", 160, 2), ("bf16", "per_layer", 16, 4), ("nvfp4", "per_layer", 160, 4)])
+def test_one_kernel_and_three_kernel_decode_agree_bitwise(fmt, pool_mode, E, T):
+    # The persistent one-kernel decode (split_decode 0) and the route / gate/up
+    # / down kernels give the same bits: ids, slots, fills, outputs, final
+    # state and counters; both match the oracle.
+    k = 4 if E >= 40 else 2
+    w = scaled(WORKLOADS["flash_next_nvfp4"], name="fused", L=3, E=E, k=k, H=512, I=192, fmt=fmt,
+               pool_mode=pool_mode, slots_per_layer=max(T * k + 3, 12), pool_bytes=0.0,
+               has_shared=fmt in ("nvfp4", "q4_0"), bias=True, streams=(T,), steps=6, rho=0.7)
+    import oracle
+    sb = oracle.slot_bytes(fmt, w.H, w.I)
+    if pool_mode == "shared":
+        w = scaled(w, pool_bytes=sb * (T * k + 6) + 5)
+    runs = {}
+    for split in (False, True):
+        st = Setup(w, split_decode=split)
+        orc = OracleRun(w, st.info["slot_bytes"])
+        xs = {l: st.hiddens(l, T, w.steps) for l in range(w.L)}
+        ys, recs = [], []
+        for s in range(w.steps):
+            for l in range(w.L):
+                y = st.forward(xs[l][s], l)
+                ids, _ = orc.route(xs[l][s], st.router[l], st.bias)
+                plan = orc.plan(l, ids, T)
+                rec = st.cache.trace_read()[0]
+                compare_trace(rec, ids, plan, l, T)
+                ys.append(y)
+                recs.append(rec)
+                if s % 3 == 0:
+                    _, _, yo = orc.layer(xs[l][s], st.router[l], st.bias, l)
+                    assert rel_l2(y, yo) <= TOL
+        info = st.cache.info()
+        calls = w.steps * w.L
+        assert (info["split_decode_calls"], info["fused_decode_calls"]) == ((calls, 0) if split else (0, calls))
+        runs[split] = (np.stack(ys), recs, st.cache.state(), st.cache.stats())
+        st.close()
+    (y0, r0, s0, c0), (y1, r1, s1, c1) = runs[False], runs[True]
+    assert np.array_equal(y0, y1)
+    for a, b in zip(r0, r1):
+        for key in ("ids", "slot_of", "hit_of", "fill_expert", "fill_slot"):
+            assert np.array_equal(a[key], b[key]), key
+    for key in s0:
+        assert np.array_equal(s0[key], s1[key]), key
+    for bkt in range(3):
+        for key in ("calls", "hits", "misses", "bytes_uploaded"):
+            assert c0["buckets"][bkt][key] == c1["buckets"][bkt][key]
+    if c0["buckets"][0]["misses"]:
+        assert c0["buckets"][0]["upload_ns"] > 0
