@@ -105,14 +105,16 @@ typedef struct {
     int32_t prefill_group;    /* experts staged per prefill group (32) */
     int32_t max_tokens;       /* largest T of any call (sizes scratch) */
     int32_t device;           /* CUDA device ordinal */
-    int32_t split_decode;     /* 0: a decode call that fits (T <= 8, T*k (+T shared) <= 48, PULL
-                                 uploads) runs as one persistent kernel, one CTA per SM with two
-                                 bounded grid barriers; 1 (default): always three kernels (route,
-                                 gate/up, down). Both give bitwise identical results. */
+    int32_t split_decode;     /* 0 (default): a decode call that fits (T <= 8, T*k (+T shared) <= 48,
+                                 PULL uploads) runs as one persistent kernel, one CTA per SM with
+                                 two bounded grid barriers, its weight tiles streamed into shared
+                                 memory by bulk copies; other calls take the three kernels.
+                                 1: always three kernels (route, gate/up, down). Both give bitwise
+                                 identical results. */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
- * max_tokens 32, upload PULL, per-layer pools, split_decode 1; shape fields
+ * max_tokens 32, upload PULL, per-layer pools, split_decode 0; shape fields
  * zero. */
 void moe_config_default(moe_config_t* cfg);
 

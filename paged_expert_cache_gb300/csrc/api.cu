@@ -139,7 +139,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->prefill_group = 32;
     cfg->max_tokens = 32;
     cfg->device = 0;
-    cfg->split_decode = 1;
+    cfg->split_decode = 0;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -482,6 +482,7 @@ moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out) {
     unsigned derr = 0;
     CK(h, cudaMemcpy(&derr, h->scr.err, sizeof derr, cudaMemcpyDeviceToHost));
     if (derr & 1u) return fail(h, MOE_ERR_TIMEOUT, "a grid barrier of the one-kernel decode path timed out");
+    if (derr & 2u) return fail(h, MOE_ERR_TIMEOUT, "a weight-slot wait of the one-kernel decode path timed out");
     return MOE_OK;
 }
 

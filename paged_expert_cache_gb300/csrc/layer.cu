@@ -8,31 +8,41 @@
 //
 // One CTA per SM, all resident at once, with two grid-wide barriers:
 //
-//   1. Each CTA holds the router rows of its experts in registers, issued
+//   1. Each CTA copies the router rows of its experts to shared memory
 //      before the wait on the preceding grid; it stages the tokens and writes
 //      its experts' logit pairs and bounds. It also copies the pool's state
 //      (stamps, keys, the layer's slot map) into shared memory: every CTA reads
-//      the state before the first barrier, and only CTA 0 writes it, after.
+//      the state before the first barrier, and only the committing CTA writes
+//      it, after.
 //   -- barrier: every logit is written.
 //   2. Every CTA ranks every token and runs the plan itself, from the same
 //      logits and the same state, so all CTAs derive the same unit
 //      descriptors in their own shared memory: no second round trip through
-//      global memory. CTA 0 alone commits the state, the fill list, the stats
-//      and the trace. Each CTA then asks L2 for the weight bytes it is about
-//      to read (bulk L2 prefetches of resident slots), and its two groups of
-//      eight warps compute (unit, 16-row tile) items of gate/up + SwiGLU; a
-//      missed unit's tiles are read from the mapped host store and written
-//      through to the slot, as in the three-kernel path.
+//      global memory. One CTA (the last) commits the state, the fill list,
+//      the stats and the trace.
+//      The CTA then knows every weight byte it will read in this call: the
+//      gate/up rows of its (unit, 16-row tile) items and the down rows of its
+//      output tiles. It streams the resident ones into a ring of shared-memory
+//      slots with bulk copies (the tensor-memory-access engine, completion on
+//      one mbarrier per slot, L2 evict-first so streamed weights do not push
+//      out the code, the router and the pool state), so HBM sees the whole
+//      call's bytes requested at once; each slot is refilled with the next
+//      piece as soon as its consumers are done. Two groups of eight warps
+//      compute gate/up + SwiGLU from the slots; a missed unit's tiles are read
+//      from the mapped host store and written through to the slot, as in the
+//      three-kernel path.
 //   -- barrier: every activation is written.
 //   3. CTA b computes output row tiles b, b + G, ... of the down projection
-//      over every unit and combines them with the router weights.
+//      over every unit from the down pieces already in its slots, and
+//      combines them with the router weights.
 //
 // The arithmetic of every step is the three-kernel path's (same per-warp
 // logit sums, same chunk split and warp order in gate/up, the same row-tile
 // down projection), so the two paths give bitwise identical results.
 //
-// Barrier waits are bounded: a wait that outlasts kBarrierTimeoutNs sets an
-// error bit the host reports as MOE_ERR_TIMEOUT, and the kernel returns.
+// Waits are bounded: a grid barrier or a slot wait that outlasts its limit
+// sets an error bit the host reports as MOE_ERR_TIMEOUT; the kernel waits
+// (again bounded) for its own copies in flight before it returns.
 #include "expert_dev.cuh"
 #include "route_dev.cuh"
 
@@ -43,24 +53,48 @@ constexpr int kLWarps = kLThreads / 32;
 constexpr int kLayerMaxTokens = 8;    // tokens per call (a unit has at most 8 pairs: one n-tile)
 constexpr int kLayerMaxPairs = 48;    // T * k (+ T for the shared expert)
 constexpr int kLayerRankWarps = 4;    // warps that rank tokens (each needs a TopkSmem)
+constexpr int kMaxSlots = 16;         // ring slots
 constexpr unsigned long long kBarrierTimeoutNs = 200ull * 1000 * 1000;
 constexpr unsigned kBarrierMaxPolls = 1u << 24;
+constexpr unsigned long long kSlotTimeoutNs = 200ull * 1000 * 1000;
+constexpr unsigned kSlotMaxPolls = 1u << 26;
 constexpr size_t kLayerSmemLimit = 224 * 1024;  // dynamic; the static variables take the rest
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+__host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
+
+// Upper bound on the bytes of one 16-row tile of a slot matrix with C
+// columns: its codes plus its scales (tile_ranges below gives the exact
+// ranges; block-FP8's scale range is rounded out to 16 bytes).
+__host__ __device__ inline size_t tile_bytes_bound(int fmt, int C) {
+    const size_t KC = (size_t)C / 64;
+    switch (fmt) {
+    case FMT_Q4_0:
+    case FMT_NVFP4: return KC * 576;
+    case FMT_FP8_B128: return KC * 1024 + align16((size_t)((C + 127) / 128) * 4) + 16;
+    default: return KC * 2048;
+    }
+}
 
 // Shared-memory layout of one call, computed the same way on host and device.
+//   persistent: unit descriptors, picks, weights, f16 tokens, slot mbarriers
+//   region A:   phase 1-2 (tokens, router rows, plan, ranking)  |  the ring
+//   region B:   gate/up partial tiles  |  down staging (activations, partials)
 struct LayerLayout {
-    size_t sd, ids, wts, xg;     // persistent: descriptors, picks, weights, f16 tokens [T+1][H+8]
-    size_t un;                   // start of the phase union
-    size_t xs, wr, plan, topk;   // phase 1-2: bf16 tokens [T][H], router rows, the plan, ranking warps
-    size_t red;                  // phase 2: gate/up partial tiles [2 groups][8 warps][2][128]
-    size_t ah, al, ps;           // phase 3: activations hi/lo, down partials
+    size_t sd, ids, wts, xg, bars, last;
+    size_t xs, wr, plan, topk;
+    size_t ring;
+    size_t red, ah, al, ps;
+    size_t gl;       // offset of the up matrix in a gate/up piece (bound of one tile)
+    size_t du;       // bytes per unit in a down piece
+    size_t slot;     // bytes per ring slot
+    int ns;          // ring slots (0: the call does not fit)
+    int m;           // units per down piece
     size_t total;
 };
 
-__host__ __device__ inline LayerLayout layer_layout(int E, int K, int k, int H, int I, int T, int has_shared,
-                                                    int rows) {
+__host__ __device__ inline LayerLayout layer_layout(int fmt, int E, int K, int k, int H, int I, int T,
+                                                    int has_shared, int rows) {
     LayerLayout L;
     const int n_ids = T * k, U = (n_ids < E ? n_ids : E) + 1, P = n_ids + (has_shared ? T : 0);
     size_t o = 0;
@@ -68,27 +102,40 @@ __host__ __device__ inline LayerLayout layer_layout(int E, int K, int k, int H, 
     L.ids = o; o = align16(o + (size_t)n_ids * 4);
     L.wts = o; o = align16(o + (size_t)n_ids * 4);
     L.xg = o; o = align16(o + (size_t)(T + 1) * (H + 8) * 2);
-    L.un = o;
-    // phases 1-2: tokens, plan, ranking
-    size_t p = o;
+    L.bars = o; o = align16(o + (size_t)kMaxSlots * 8);
+    L.last = o; o = align128(o + (size_t)kMaxSlots * 4);
+    const size_t a0 = o;
+    // phases 1-2: tokens, router rows, plan, ranking
+    size_t p = a0;
     L.xs = p; p = align16(p + (size_t)T * H * 2);
     L.wr = p; p = align16(p + (size_t)rows * H * 2);
     L.plan = p; p = align16(p + plan_layout(nullptr, E, K, n_ids, U, P).bytes);
     L.topk = p; p = align16(p + (size_t)(T < kLayerRankWarps ? T : kLayerRankWarps) * topk_bytes_per_warp(E));
-    size_t end = p;
-    // gate/up
-    L.red = o;
-    p = align16(o + (size_t)2 * 8 * 2 * 128 * 4);
-    if (p > end) end = p;
-    // down
+    const size_t phase12 = p - a0;
+    // region B: gate/up partials, or the down staging
     const size_t ld = (size_t)I + 8;
-    L.ah = o;
-    L.al = align16(L.ah + (size_t)(P + 1) * ld * 2);
-    L.ps = align16(L.al + (size_t)(P + 1) * ld * 2);
-    p = L.ps + down_rows_work_bytes(I, P) - 2 * (size_t)(P + 1) * ld * 2;
-    p = align16(p);
-    if (p > end) end = p;
-    L.total = end;
+    const size_t red_bytes = (size_t)2 * 8 * 2 * 128 * 4;
+    const size_t act_bytes = align16((size_t)(P + 1) * ld * 2);
+    const size_t ps_bytes = down_rows_work_bytes(I, P) - 2 * (size_t)(P + 1) * ld * 2;
+    const size_t down_bytes = 2 * act_bytes + align16(ps_bytes);
+    const size_t b_bytes = align128(red_bytes > down_bytes ? red_bytes : down_bytes);
+    // the ring
+    L.gl = tile_bytes_bound(fmt, H);
+    L.du = align128(tile_bytes_bound(fmt, I));
+    L.slot = align128(2 * L.gl > L.du ? 2 * L.gl : L.du);
+    L.m = (int)(L.slot / L.du);
+    const size_t avail = kLayerSmemLimit > a0 + b_bytes ? kLayerSmemLimit - a0 - b_bytes : 0;
+    size_t ns = avail / L.slot;
+    if (ns > (size_t)kMaxSlots) ns = kMaxSlots;
+    L.ns = (int)ns;
+    const size_t a_bytes = align128(phase12 > ns * L.slot ? phase12 : ns * L.slot);
+    L.ring = a0;
+    L.red = a0 + a_bytes;
+    L.ah = L.red;
+    L.al = L.ah + act_bytes;
+    L.ps = L.al + act_bytes;
+    L.total = L.red + b_bytes;
+    if (L.total > kLayerSmemLimit) L.ns = 0;
     return L;
 }
 
@@ -135,14 +182,68 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
 }
-
-// Asks L2 for [p, p + bytes) of device memory (16-byte aligned start and
-// size); the copy runs in the background.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;\n" ::: "memory");
 }
 
-// The byte range of row tile rt of a slot matrix (R rows, C cols): the codes
+// ---------------------------------------------------------------------------
+// Slot ring: mbarriers and bulk copies (sm_90+ PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
+}
+// Arrives and adds `bytes` to the transaction count the phase waits for.
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase of the given parity to complete; false if the wait
+// gave up (time or poll limit).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (unsigned it = 0; it < kSlotMaxPolls; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kSlotTimeoutNs) break;
+    }
+    return false;
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+// Bulk copy global -> this CTA's shared memory (16-byte aligned addresses,
+// size a multiple of 16), completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+// The byte ranges of row tile rt of a slot matrix (R rows, C cols): the codes
 // of its chunks, then the scales they use (rounded out to 16 bytes; both stay
 // inside the matrix's 16-byte padded extent). Returns the number of ranges.
 template <int FMT>
@@ -166,17 +267,44 @@ __device__ __forceinline__ int tile_ranges(int R, int C, int rt, uint64_t (&off)
     } else {
         off[0] = (uint64_t)rt * KC * 2048;
         len[0] = (uint32_t)KC * 2048;
+        len[1] = 0;
         return 1;
     }
 }
 
-// 16-byte asynchronous copy global -> shared (completed by cp_async_wait).
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+// Lane's share of chunk kc of a 16-row tile staged in shared memory by
+// tile_ranges (codes at `t`, scales at `t + len0`; `soff` is the block-FP8
+// scale range's start within its first 16 bytes). Same fragments as
+// load_chunk reads from the slot.
+template <int FMT>
+__device__ __forceinline__ void smem_chunk(const uint8_t* t, uint32_t len0, uint32_t soff, int kc, int lane,
+                                           Chunk<FMT>& ch) {
+    if constexpr (FMT == FMT_Q4_0 || FMT == FMT_NVFP4) {
+        ch.q = *reinterpret_cast<const uint4*>(t + (size_t)kc * 512 + lane * 16);
+        ch.sc = *reinterpret_cast<const uint2*>(t + len0 + (size_t)kc * 64 + (lane >> 2) * 8);
+    } else if constexpr (FMT == FMT_FP8_B128) {
+        const uint8_t* q = t + (size_t)kc * 1024 + lane * 32;
+        ch.q0 = *reinterpret_cast<const uint4*>(q);
+        ch.q1 = *reinterpret_cast<const uint4*>(q + 16);
+        ch.sc = *reinterpret_cast<const float*>(t + len0 + soff + (size_t)(kc >> 1) * 4);
+    } else {
+        const uint8_t* q = t + (size_t)kc * 2048 + lane * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ch.q[i] = *reinterpret_cast<const uint4*>(q + 16 * i);
+    }
 }
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_all;\n" ::: "memory");
+
+// Start of the block-FP8 scale range of row tile rt within its 16-byte
+// rounded copy (0 for the other formats).
+template <int FMT>
+__device__ __forceinline__ uint32_t scale_soff(int R, int C, int rt) {
+    if constexpr (FMT == FMT_FP8_B128) {
+        const int nct = (C + 127) / 128;
+        const uint64_t s0 = (uint64_t)R * C + (uint64_t)((rt * 16) / 128) * nct * 4;
+        return (uint32_t)(s0 & 15ull);
+    } else {
+        return 0u;
+    }
 }
 
 // B fragments of the four k-steps of chunk kc, each lane reading its own
@@ -191,12 +319,173 @@ __device__ __forceinline__ void group_sync(int group) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(group + 1), "r"(256) : "memory");
 }
 
+// The pieces a CTA streams through its ring, in order: its gate/up items
+// (unit, row tile) it = b + G j, then for each of its output row tiles
+// rt = b + G r the down rows of units u0 .. u0 + m - 1.
+struct Pieces {
+    int b, G, RT, n_units, n_gu, n_rt, dpr, n;
+};
+
+__device__ __forceinline__ Pieces make_pieces(int b, int G, int RT, int RTD, int n_units, int m) {
+    Pieces q;
+    q.b = b;
+    q.G = G;
+    q.RT = RT;
+    q.n_units = n_units;
+    const int n_items = n_units * RT;
+    q.n_gu = n_items > b ? (n_items - 1 - b) / G + 1 : 0;
+    q.n_rt = RTD > b ? (RTD - 1 - b) / G + 1 : 0;
+    q.dpr = (n_units + m - 1) / m;
+    q.n = q.n_gu + q.n_rt * q.dpr;
+    return q;
+}
+
+// Issues piece i into slot i % ns: bulk copies of its resident bytes, with one
+// arrival on the slot's mbarrier (missed units' bytes are not copied: their
+// consumers read the host store or the slot directly). One thread.
+template <int FMT>
+__device__ __noinline__ void issue_piece(int i, const Pieces& q, const LayerLayout& L, const UnitDesc* sd, uint8_t* smem, int H,
+                            int I, uint64_t pol) {
+    const int slot = i % L.ns;
+    const uint32_t bar = smem_u32(smem + L.bars) + slot * 8;
+    const uint32_t dst = smem_u32(smem + L.ring) + (uint32_t)(slot * L.slot);
+    reinterpret_cast<int*>(smem + L.last)[slot] = i;
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    uint64_t off[2];
+    uint32_t len[2];
+    if (i < q.n_gu) {
+        const int it = q.b + q.G * i, u = it / q.RT, rt = it - u * q.RT;
+        const UnitDesc& d = sd[u];
+        if (d.dst) {
+            mbar_arrive(bar);
+            return;
+        }
+        const int nr = tile_ranges<FMT>(I, H, rt, off, len);
+        uint32_t total = 0;
+        for (int r = 0; r < nr; ++r) total += len[r];
+        mbar_arrive_tx(bar, 2 * total);
+        for (int mat = 0; mat < 2; ++mat) {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(d.src) + mat * mgu;
+            uint32_t o = dst + (uint32_t)(mat * L.gl);
+            for (int r = 0; r < nr; ++r) {
+                bulk_g2s(o, src + off[r], len[r], bar, pol);
+                o += len[r];
+            }
+        }
+    } else {
+        const int di = i - q.n_gu, r = di / q.dpr, u0 = (di - r * q.dpr) * L.m;
+        const int rt = q.b + q.G * r;
+        const int nr = tile_ranges<FMT>(H, I, rt, off, len);
+        uint32_t per = 0;
+        for (int j = 0; j < nr; ++j) per += len[j];
+        uint32_t total = 0;
+        for (int v = 0; v < L.m && u0 + v < q.n_units; ++v)
+            if (!sd[u0 + v].dst) total += per;
+        if (!total) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_tx(bar, total);
+        for (int v = 0; v < L.m && u0 + v < q.n_units; ++v) {
+            const UnitDesc& d = sd[u0 + v];
+            if (d.dst) continue;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(d.src) + 2 * mgu;
+            uint32_t o = dst + (uint32_t)(v * L.du);
+            for (int j = 0; j < nr; ++j) {
+                bulk_g2s(o, src + off[j], len[j], bar, pol);
+                o += len[j];
+            }
+        }
+    }
+}
+
+// Waits (bounded) for the last piece issued into every slot; used before the
+// CTA exits so no copy is in flight into its shared memory.
+__device__ __forceinline__ void drain_ring(const LayerLayout& L, uint8_t* smem, int n_issued_max) {
+    if (threadIdx.x != 0) return;
+    const int* last = reinterpret_cast<const int*>(smem + L.last);
+    const uint32_t bars = smem_u32(smem + L.bars);
+    for (int sl = 0; sl < L.ns; ++sl) {
+        const int i = last[sl];
+        if (i >= 0 && i < n_issued_max) mbar_wait(bars + sl * 8, (uint32_t)((i / L.ns) & 1));
+    }
+}
+
+
+// Gate/up of one 16-row tile of a missed unit, read from the mapped host store
+// (Wg: gate; up follows at the matrix stride) and written through to its slot
+// (Dg) as it is read, by one group of eight warps (gw: the warp in the group,
+// gtid: the thread). Out of line: calls with misses are bound by the host
+// link, and the all-hit path keeps a short instruction stream.
+template <int FMT>
+__device__ __noinline__ void gateup_pull(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
+                                         int lane, const uint16_t* brow, float (&ag)[4], float (&au)[4]) {
+    constexpr int CIF = FMT == FMT_BF16 ? 1 : 2;  // chunks in flight
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    const uint8_t* Wu = Wg + mgu;
+    uint8_t* Du = Dg + mgu;
+    const int KC = H / 64, cpw = (KC + 7) / 8;
+    if (rt == 0) {
+        copy_matrix_tail<FMT>(Wg, Dg, I, H, gtid, 256);
+        copy_matrix_tail<FMT>(Wu, Du, I, H, gtid, 256);
+    }
+    for (int c0 = 0; c0 < cpw; c0 += CIF) {
+        Chunk<FMT> cg[CIF], cu[CIF];
+#pragma unroll
+        for (int i = 0; i < CIF; ++i) {
+            const int kc = gw * cpw + c0 + i;
+            if (c0 + i < cpw && kc < KC) {
+                load_chunk<FMT>(Wg, Dg, I, H, rt, kc, lane, cg[i]);
+                load_chunk<FMT>(Wu, Du, I, H, rt, kc, lane, cu[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < CIF; ++i) {
+            const int kc = gw * cpw + c0 + i;
+            if (c0 + i < cpw && kc < KC) {
+                uint32_t bb[1][4][2];
+                load_b_row(brow, kc, lane, bb[0]);
+                mma_chunk<FMT, 1>(cg[i], bb, ag);
+                mma_chunk<FMT, 1>(cu[i], bb, au);
+            }
+        }
+    }
+}
+
+// Row tile rt's share of a missed record's down matrix, copied from the host
+// store to the slot by one group (256 threads), so the whole record crosses
+// the host link in the gate/up pass.
+template <int FMT>
+__device__ __noinline__ void pull_down_share(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid) {
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    const int RT = I / 16;
+    const uint64_t mdn = matrix_stride(FMT, H, I);
+    const uint64_t nvec = mdn / 16, per = (nvec + RT - 1) / RT;
+    const uint64_t v0 = (uint64_t)rt * per, v1 = v0 + per < nvec ? v0 + per : nvec;
+    const uint8_t* src = Wg + 2 * mgu;
+    uint8_t* dst = Dg + 2 * mgu;
+    constexpr int kBatch = 4;
+    for (uint64_t v = v0 + gtid; v < v1; v += 256ull * kBatch) {
+        uint4 buf[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint64_t vi = v + (uint64_t)i * 256;
+            if (vi < v1) buf[i] = ldg_stream(src + vi * 16);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint64_t vi = v + (uint64_t)i * 256;
+            if (vi < v1) stg_stream(dst + vi * 16, buf[i]);
+        }
+    }
+}
 
 template <int FMT>
 __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, RouteArgs a, float* __restrict__ out) {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ unsigned long long clk;
     __shared__ int rerank;
+    __shared__ int slot_err;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
     const int E = c.E, H = c.H, I = c.I, k = c.k, T = a.T;
@@ -205,12 +494,19 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     const int P = n_ids + (c.has_shared ? T : 0);
     const int pool = c.pool_mode ? 0 : a.layer;
     const int rows = (E + G - 1) / G;
-    const LayerLayout L = layer_layout(E, c.K, k, H, I, T, c.has_shared, rows);
+    const LayerLayout L = layer_layout(FMT, E, c.K, k, H, I, T, c.has_shared, rows);
     UnitDesc* sd = reinterpret_cast<UnitDesc*>(smem + L.sd);
     int* sids = reinterpret_cast<int*>(smem + L.ids);
     float* swts = reinterpret_cast<float*>(smem + L.wts);
     uint16_t* xg = reinterpret_cast<uint16_t*>(smem + L.xg);
     const int ldx = H + 8;
+    const uint32_t bars = smem_u32(smem + L.bars);
+    if (tid < kMaxSlots) reinterpret_cast<int*>(smem + L.last)[tid] = -1;
+    if (tid == 0) {
+        for (int i = 0; i < L.ns; ++i) mbar_init(bars + i * 8, 1);
+        fence_mbar_init();
+        slot_err = 0;
+    }
 
     // ---- 1. logits ---------------------------------------------------------
     // warp j of CTA b owns expert b + j G; its router row does not depend on
@@ -229,7 +525,8 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     {
         // one round of asynchronous copies: the tokens and the pool's state
         // (stamps, keys, the layer's slot map, NVFP4 global scales), read by
-        // every CTA before the first barrier (only CTA 0 writes them, after)
+        // every CTA before the first barrier (only the committing CTA writes
+        // them, after)
         const unsigned long long* lu = c.last_use + (size_t)pool * c.K;
         const int* kof = c.key_of + (size_t)pool * c.K;
         const int* smap = c.slot_map + (size_t)a.layer * E;
@@ -274,17 +571,11 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         }
         for (int i = tid; i < ldx / 2; i += kLThreads) reinterpret_cast<uint32_t*>(xg + (size_t)T * ldx)[i] = 0u;
     }
-    if (e_mine < E) {
-        uint4 wv[kRouterMaxVec];
-#pragma unroll
-        for (int i = 0; i < kRouterMaxVec; ++i)
-            if (i < H / 256) wv[i] = *reinterpret_cast<const uint4*>(wr + lane * 8 + i * 256);
-        for (int t = 0; t < T; ++t)
-            router_logits_warp<1>(c, a, xs + (size_t)t * H, t, 1, e_mine, wv, s.logits, s.bounds);
-    }
-    if (!grid_barrier(s.grid_bar, s.err, phase)) return;
+    if (e_mine < E)
+        for (int t = 0; t < T; ++t) router_logit_row(c, a, xs + (size_t)t * H, wr, t, e_mine, s.logits, s.bounds);
+    if (!grid_barrier(s.grid_bar, s.err, phase)) return;  // nothing is in flight yet
 
-    // ---- 2. top-k and plan in every CTA, then gate/up ---------------------
+    // ---- 2. top-k and plan in every CTA ----------------------------------
     {
         const int nrw = min(T, kLayerRankWarps);
         if (warp < nrw) {
@@ -293,7 +584,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         }
     }
     __syncthreads();
-    const bool commit = b == 0;
+    const bool commit = b == G - 1;
     if (commit) {
         for (int i = tid; i < n_ids; i += kLThreads) {
             s.ids[i] = sids[i];
@@ -304,100 +595,121 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             if (rerank) c.stats[15] += 1;
         }
     }
-    plan_small(c, s, a, m, clk, sids, sd, commit);
-    const int n_units = m.scal[0] + (c.has_shared ? 1 : 0);
-    __syncthreads();  // the gate/up scratch below overlaps the plan's shared memory
-    const int RT = I / 16, KC = H / 64;
-    const int n_items = n_units * RT;
-    const uint64_t mgu = matrix_stride(FMT, I, H);
-    // L2 prefetch of the resident bytes this CTA reads: its gate/up items,
-    // then its down row tiles of every unit
-    {
-        const int n_mine = n_items > b ? (n_items - b + G - 1) / G : 0;
-        for (int q = tid; q < n_mine * 2; q += kLThreads) {
-            const int it = b + G * (q >> 1), u = it / RT, rt = it - u * RT;
-            const UnitDesc& d = sd[u];
-            if (d.dst) continue;  // a miss: read from the host store
-            const uint8_t* M = reinterpret_cast<const uint8_t*>(d.src) + (q & 1) * mgu;
-            uint64_t off[2];
-            uint32_t len[2];
-            const int nr = tile_ranges<FMT>(I, H, rt, off, len);
-            for (int r = 0; r < nr; ++r) prefetch_l2(M + off[r], len[r]);
+    // A single token whose picks are all resident needs no cache transaction
+    // to find its weights: unit j is pick j, read in place from its slot (the
+    // descriptors the full plan gives such a call). The committing CTA still
+    // runs the full plan, which also touches the slots and counts the hits.
+    __shared__ int fast;
+    if (warp == 0) {
+        int ok = 0;
+        if (T == 1 && !commit) {
+            const int sl = lane < k ? m.smap[sids[lane]] : 0;
+            ok = __all_sync(0xffffffffu, sl >= 0);
+            if (ok && lane <= k) {
+                UnitDesc d;
+                d.pstart = 0;
+                d.np = 1;
+#pragma unroll
+                for (int j = 1; j < 8; ++j) d.pair8[j] = -1;
+                d.pair8[0] = lane;
+                d.dst = 0;
+                d.hit = 1;
+                if (lane < k) {
+                    const int e = sids[lane];
+                    d.expert = e;
+                    d.slot = sl;
+                    d.src = (uint64_t)(c.pool + ((size_t)pool * c.K + sl) * c.slot_stride);
+                    for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[e * 3 + j] : 1.0f;
+                } else {
+                    d.expert = -1;
+                    d.slot = -1;
+                    d.src = (uint64_t)(c.shared_w + (size_t)a.layer * c.slot_stride);
+                    for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[E * 3 + j] : 1.0f;
+                }
+                if (lane < k || c.has_shared) sd[lane] = d;
+            }
         }
-        const int RTD = H / 16;
-        const int n_dt = RTD > b ? (RTD - b + G - 1) / G : 0;
-        for (int q = tid; q < n_dt * n_units; q += kLThreads) {
-            const int u = q % n_units, rt = b + G * (q / n_units);
-            const UnitDesc& d = sd[u];
-            if (d.dst) continue;
-            const uint8_t* M = reinterpret_cast<const uint8_t*>(d.src) + 2 * mgu;
-            uint64_t off[2];
-            uint32_t len[2];
-            const int nr = tile_ranges<FMT>(H, I, rt, off, len);
-            for (int r = 0; r < nr; ++r) prefetch_l2(M + off[r], len[r]);
-        }
+        if (lane == 0) fast = ok;
     }
-    // gate/up + SwiGLU: group g (warps 8g .. 8g+7) takes items b + G j for
-    // j = g, g + 2, ...; the K split over the group's warps, the chunk batches
-    // and the warp-ordered sum are the gate/up kernel's
+    __syncthreads();
+    int n_units;
+    if (fast) {
+        n_units = k + (c.has_shared ? 1 : 0);
+    } else {
+        plan_small(c, s, a, m, clk, sids, sd, commit);
+        n_units = m.scal[0] + (c.has_shared ? 1 : 0);
+    }
+    __syncthreads();  // the ring below overlaps the plan's shared memory
+
+    // ---- 3. stream the call's weight bytes; gate/up + SwiGLU ---------------
+    const int RT = I / 16, KC = H / 64, RTD = H / 16, KCD = I / 64;
+    const uint64_t mgu = matrix_stride(FMT, I, H);
+    const Pieces q = make_pieces(b, G, RT, RTD, n_units, L.m);
+    const uint64_t pol = policy_evict_first();
+    if (tid == 0) {
+        // the ring reuses shared memory the generic proxy wrote in phases 1-2
+        fence_proxy_async();
+        for (int i = 0; i < q.n && i < L.ns; ++i) issue_piece<FMT>(i, q, L, sd, smem, H, I, pol);
+    }
+    const uint8_t* ring = smem + L.ring;
     {
+        // group g (warps 8g .. 8g+7) takes items j = g, g + 2, ...; the K split
+        // over the group's warps and the warp-ordered sum are the gate/up
+        // kernel's
         const int grp = warp >> 3, gw = warp & 7, gtid = tid & 255;
         float* red = reinterpret_cast<float*>(smem + L.red) + (size_t)grp * 8 * 2 * 128;
         const int cpw = (KC + 7) / 8;
-        // chunks a warp keeps in flight: fewer than the gate/up kernel's, to
-        // stay within 128 registers; the L2 prefetch above hides the rest
-        constexpr int CIF = FMT == FMT_BF16 ? 1 : 2;
-        for (int j = grp; b + G * j < n_items; j += 2) {
+        for (int j = grp; j < q.n_gu; j += 2) {
             const int it = b + G * j, u = it / RT, rt = it - u * RT;
             const UnitDesc d = sd[u];
+            const int slot = j % L.ns;
             const uint8_t* Wg = reinterpret_cast<const uint8_t*>(d.src);
             const uint8_t* Wu = Wg + mgu;
             uint8_t* Dg = d.dst ? reinterpret_cast<uint8_t*>(d.dst) : nullptr;
-            uint8_t* Du = Dg ? Dg + mgu : nullptr;
-            if (Dg && gtid == 0) atomicMin(s.copy_t0, globaltimer_ns());
-            if (Dg && rt == 0) {
-                copy_matrix_tail<FMT>(Wg, Dg, I, H, gtid, 256);
-                copy_matrix_tail<FMT>(Wu, Du, I, H, gtid, 256);
-            }
             const int np = d.np;
             // this lane's token row of the B tile (zero row past the unit's pairs)
             const int col = lane & 7;
             const int tok = col < np ? pair_token(pair_at(s, d, col), T, k) : T;
             const uint16_t* brow = xg + (size_t)tok * ldx;
             float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int c0 = 0; c0 < cpw; c0 += CIF) {
-                Chunk<FMT> cg[CIF], cu[CIF];
-#pragma unroll
-                for (int i = 0; i < CIF; ++i) {
-                    const int kc = gw * cpw + c0 + i;
-                    if (c0 + i < cpw && kc < KC) {
-                        load_chunk<FMT>(Wg, Dg, I, H, rt, kc, lane, cg[i]);
-                        load_chunk<FMT>(Wu, Du, I, H, rt, kc, lane, cu[i]);
-                    }
+            if (!Dg) {
+                // resident: the tile is (or will be) in slot j % ns
+                if (!mbar_wait(bars + slot * 8, (uint32_t)((j / L.ns) & 1))) slot_err = 1;
+                const uint8_t* pg = ring + (size_t)slot * L.slot;
+                const uint8_t* pu = pg + L.gl;
+                const uint32_t len0 = (uint32_t)KC * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
+                const uint32_t soff = scale_soff<FMT>(I, H, rt);
+                for (int c0 = 0; c0 < cpw; ++c0) {
+                    const int kc = gw * cpw + c0;
+                    if (kc >= KC) break;
+                    Chunk<FMT> cg, cu;
+                    smem_chunk<FMT>(pg, len0, soff, kc, lane, cg);
+                    smem_chunk<FMT>(pu, len0, soff, kc, lane, cu);
+                    uint32_t bb[1][4][2];
+                    load_b_row(brow, kc, lane, bb[0]);
+                    mma_chunk<FMT, 1>(cg, bb, ag);
+                    mma_chunk<FMT, 1>(cu, bb, au);
                 }
-#pragma unroll
-                for (int i = 0; i < kMaxChunksInFlight; ++i) {
-                    const int kc = gw * cpw + c0 + i;
-                    if (c0 + i < cpw && kc < KC) {
-                        uint32_t bb[1][4][2];
-                        load_b_row(brow, kc, lane, bb[0]);
-                        mma_chunk<FMT, 1>(cg[i], bb, ag);
-                        mma_chunk<FMT, 1>(cu[i], bb, au);
-                    }
-                }
+            } else {
+                // missed: read the tile from the mapped host store over the
+                // host link and write it through to the slot
+                if (gtid == 0) atomicMin(s.copy_t0, globaltimer_ns());
+                gateup_pull<FMT>(Wg, Dg, I, H, rt, gtid, gw, lane, brow, ag, au);
             }
-            const int g = lane >> 2, q = lane & 3;
+            const int g = lane >> 2, qd = lane & 3;
             float* rg = red + (size_t)(gw * 2) * 128;
             float* ru = rg + 128;
-            rg[g * 8 + 2 * q] = ag[0];
-            rg[g * 8 + 2 * q + 1] = ag[1];
-            rg[(g + 8) * 8 + 2 * q] = ag[2];
-            rg[(g + 8) * 8 + 2 * q + 1] = ag[3];
-            ru[g * 8 + 2 * q] = au[0];
-            ru[g * 8 + 2 * q + 1] = au[1];
-            ru[(g + 8) * 8 + 2 * q] = au[2];
-            ru[(g + 8) * 8 + 2 * q + 1] = au[3];
+            rg[g * 8 + 2 * qd] = ag[0];
+            rg[g * 8 + 2 * qd + 1] = ag[1];
+            rg[(g + 8) * 8 + 2 * qd] = ag[2];
+            rg[(g + 8) * 8 + 2 * qd + 1] = ag[3];
+            ru[g * 8 + 2 * qd] = au[0];
+            ru[g * 8 + 2 * qd + 1] = au[1];
+            ru[(g + 8) * 8 + 2 * qd] = au[2];
+            ru[(g + 8) * 8 + 2 * qd + 1] = au[3];
             group_sync(grp);
+            // the slot is consumed: refill it with the piece ns ahead
+            if (gtid == 0 && j + L.ns < q.n) issue_piece<FMT>(j + L.ns, q, L, sd, smem, H, I, pol);
             if (gtid < 128) {
                 const int row = gtid >> 3, cc = gtid & 7;
                 float gs = 0.f, us = 0.f;
@@ -413,33 +725,19 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             }
             if (Dg) {
                 // this item's share of the missed record's down matrix
-                const uint64_t mdn = matrix_stride(FMT, H, I);
-                const uint64_t nvec = mdn / 16, per = (nvec + RT - 1) / RT;
-                const uint64_t v0 = (uint64_t)rt * per, v1 = v0 + per < nvec ? v0 + per : nvec;
-                const uint8_t* src = Wg + 2 * mgu;
-                uint8_t* dst = Dg + 2 * mgu;
-                constexpr int kBatch = 4;
-                for (uint64_t v = v0 + gtid; v < v1; v += 256ull * kBatch) {
-                    uint4 buf[kBatch];
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const uint64_t vi = v + (uint64_t)i * 256;
-                        if (vi < v1) buf[i] = ldg_stream(src + vi * 16);
-                    }
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const uint64_t vi = v + (uint64_t)i * 256;
-                        if (vi < v1) stg_stream(dst + vi * 16, buf[i]);
-                    }
-                }
+                pull_down_share<FMT>(Wg, Dg, I, H, rt, gtid);
                 if (gtid == 0) atomicMax(s.copy_t1, globaltimer_ns());
             }
             group_sync(grp);
         }
     }
-    if (!grid_barrier(s.grid_bar, s.err, phase)) return;
+    if (!grid_barrier(s.grid_bar, s.err, phase)) {
+        __syncthreads();
+        drain_ring(L, smem, q.n);
+        return;
+    }
 
-    // ---- 3. down projection + combine by row tiles -------------------------
+    // ---- 4. down projection + combine by row tiles -------------------------
     if (commit && tid == 0) {
         // every miss of the call has been streamed: book the time
         const unsigned long long t1 = atomicAdd(s.copy_t1, 0ull);
@@ -450,15 +748,92 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             *s.copy_t1 = 0ull;
         }
     }
-    const int RTD = H / 16;
-    if (b < RTD) {
+    if (q.n_rt > 0) {
         uint16_t* ah = reinterpret_cast<uint16_t*>(smem + L.ah);
         uint16_t* al = reinterpret_cast<uint16_t*>(smem + L.al);
         float* ps = reinterpret_cast<float*>(smem + L.ps);
+        const int ld = I + 8;
+        const int ncg = (KCD + kDRChunks - 1) / kDRChunks;
+        const uint32_t len0 = (uint32_t)KCD * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
         down_stage_act<FMT>(s, P, I, ah, al);
         __syncthreads();
-        for (int rt = b; rt < RTD; rt += G) down_rows_tile<FMT>(c, s, sd, n_units, T, rt, ah, al, ps, swts, out);
+        const int g = lane >> 2, qd = lane & 3;
+        for (int r = 0; r < q.n_rt; ++r) {
+            const int rt = b + G * r;
+            const uint32_t soff = scale_soff<FMT>(H, I, rt);
+            for (int pc = 0; pc < q.dpr; ++pc) {
+                const int i = q.n_gu + r * q.dpr + pc;
+                const int slot = i % L.ns;
+                if (!mbar_wait(bars + slot * 8, (uint32_t)((i / L.ns) & 1))) slot_err = 1;
+                const int u0 = pc * L.m;
+                const int nup = min(L.m, n_units - u0);
+                const uint8_t* pd = ring + (size_t)slot * L.slot;
+                for (int itm = warp; itm < nup * ncg; itm += kLWarps) {
+                    const int v = itm / ncg, cgi = itm - v * ncg;
+                    const UnitDesc& d = sd[u0 + v];
+                    const int col = lane & 7;
+                    const int pr = col < d.np ? d.pair8[col] : P;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ci = 0; ci < kDRChunks; ++ci) {
+                        const int kc = cgi * kDRChunks + ci;
+                        if (kc >= KCD) break;
+                        Chunk<FMT> ch;
+                        if (d.dst) {
+                            // a missed record: written to its slot by the gate/up pass
+                            load_chunk_cg<FMT>(reinterpret_cast<const uint8_t*>(d.dst) + 2 * mgu, H, I, rt, kc, lane, ch);
+                        } else {
+                            smem_chunk<FMT>(pd + (size_t)v * L.du, len0, soff, kc, lane, ch);
+                        }
+                        uint32_t bf[2][4][2];
+                        const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                        const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                        ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
+                        ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
+                        ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
+                        ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
+                        mma_chunk<FMT, 2>(ch, bf, acc);
+                    }
+                    const float gd = d.g[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            const int cc = 2 * qd + c2;
+                            if (cc < d.np) {
+                                const int pair = d.pair8[cc];
+                                ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+                // the slot is consumed: refill it with the piece ns ahead
+                if (tid == 0 && i + L.ns < q.n) issue_piece<FMT>(i + L.ns, q, L, sd, smem, H, I, pol);
+            }
+            for (int i = tid; i < T * 16; i += kLThreads) {
+                const int t = i >> 4, row = i & 15;
+                float y = 0.f;
+                for (int j = 0; j < k; ++j) {
+                    const int pair = t * k + j;
+                    float v = 0.f;
+                    for (int cgi = 0; cgi < ncg; ++cgi) v += ps[((size_t)cgi * P + pair) * 16 + row];
+                    y = fmaf(swts[pair], v, y);
+                }
+                if (c.has_shared) {
+                    const int pair = T * k + t;
+                    float v = 0.f;
+                    for (int cgi = 0; cgi < ncg; ++cgi) v += ps[((size_t)cgi * P + pair) * 16 + row];
+                    y += v;
+                }
+                out[(size_t)t * H + (size_t)rt * 16 + row] = y;
+            }
+            __syncthreads();
+        }
     }
+    __syncthreads();
+    if (tid == 0 && slot_err) atomicOr(s.err, 2u);
+    drain_ring(L, smem, q.n);
 }
 
 // ---------------------------------------------------------------------------
@@ -483,8 +858,8 @@ size_t layer_smem_bytes(const CacheDev& c, int T) {
     const int G = layer_ctas();
     // every expert needs a warp of some CTA
     if (P > kLayerMaxPairs || G <= 0 || (c.E + G - 1) / G > kLWarps) return 0;
-    const size_t b = layer_layout(c.E, c.K, c.k, c.H, c.I, T, c.has_shared, (c.E + G - 1) / G).total;
-    return b <= kLayerSmemLimit ? b : 0;
+    const LayerLayout L = layer_layout(c.fmt, c.E, c.K, c.k, c.H, c.I, T, c.has_shared, (c.E + G - 1) / G);
+    return L.ns >= 1 && L.total <= kLayerSmemLimit ? L.total : 0;
 }
 
 template <int FMT>

@@ -174,6 +174,65 @@ static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a,
     }
 }
 
+// The same logit and bound for one token, with the router row staged in
+// shared memory (row: the row's first element, this lane reading vectors
+// lane*8 + i*256 as router_logits_warp does) and a rolled loop over the
+// vectors: the same operations in the same order, so the same pair and bound,
+// from a short instruction stream (code that runs once per call is fetched
+// once per call).
+static __device__ void router_logit_row(const CacheDev& c, const RouteArgs& a, const uint16_t* xs, const uint16_t* row,
+                                        int t, int e, float2* logits, float* bounds) {
+    const int H = c.H, E = c.E, lane = threadIdx.x & 31;
+    float hi = 0.f, lo = 0.f, ab = 0.f;
+    const int nvec = H / 256;
+#pragma unroll 1
+    for (int i = 0; i < nvec; ++i) {
+        const int cb = lane * 8 + i * 256;
+        const uint4 wq = *reinterpret_cast<const uint4*>(row + cb);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + cb);
+        const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
+                             bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
+        const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                             bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float p = __fmul_rn(xf[j], wf[j]);
+            float sum, err;
+            two_sum(hi, p, sum, err);
+            hi = sum;
+            lo = __fadd_rn(lo, err);
+            ab = __fadd_rn(ab, fabsf(p));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+        float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+        float oa = __shfl_xor_sync(0xffffffffu, ab, off);
+        float sum, err;
+        two_sum(hi, oh, sum, err);
+        hi = sum;
+        lo = __fadd_rn(__fadd_rn(lo, ol), err);
+        ab = __fadd_rn(ab, oa);
+    }
+    if (lane == 0) {
+        // the bound of router_logits_warp
+        const float n = (float)(H / 32 + 16);
+        const float g = n * 0x1p-24f / (1.0f - n * 0x1p-24f);
+        float2 z = norm_pair(hi, lo);
+        if (a.bias) {
+            float sh, se;
+            two_sum(z.x, a.bias[e], sh, se);
+            z = norm_pair(sh, __fadd_rn(se, z.y));
+        }
+        const float S = ab * (1.0f + 2.0f * g);
+        const float beta = (2.0f * (g * g * S + (float)H * 0x1p-52f * S + 0x1p-44f * fabsf(z.x)) +
+                            (float)H * 0x1p-126f * 0x1p-22f) * (1.0f + 0x1p-20f);
+        logits[(size_t)t * E + e] = z;
+        bounds[(size_t)t * E + e] = beta;
+    }
+}
+
 // Logits of one CTA's experts for one CTA's NT tokens, with their bounds.
 template <int NT>
 static __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_t* smem, float2* logits,
@@ -256,7 +315,7 @@ __device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
 }
 
 // Top-k of token t by one warp; writes ids and weights of the token.
-static __device__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
+static __device__ __noinline__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
                            int* rerank_flag, int* ids_out, float* wts_out) {
     const int E = c.E, k = c.k, lane = threadIdx.x & 31;
     stage_cg<float2>(w.z, s.logits + (size_t)t * E, E, lane, 32);
@@ -580,7 +639,7 @@ __host__ __device__ inline PlanSmem plan_layout(uint8_t* base, int E, int K, int
     return m;
 }
 
-static __device__ void write_trace(const CacheDev& c, const Scratch& s, int layer, int T, int n_ids, int n_hit,
+static __device__ __noinline__ void write_trace(const CacheDev& c, const Scratch& s, int layer, int T, int n_ids, int n_hit,
                             int n_fill, int n_uniq) {
     // thread 0 only
     unsigned long long idx = *c.trace_count;

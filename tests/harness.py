@@ -31,7 +31,7 @@ def pool_slots(w, slot_bytes, K=None):
 class Setup:
     """A GPU cache plus the workload's device inputs."""
 
-    def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, split_decode=True):
+    def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, split_decode=False):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
