@@ -282,6 +282,10 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.tiles_done, 1);
     DA(s.grid_bar, 1);
     DA(s.err, 1);
+    if (h->maxT > c.max_cache_tokens) {
+        DA(s.gemm_items, moe::gemm_max_items(P, U));
+        DA(s.gemm_count, 1);
+    }
 #undef DA
     h->scratch_bytes = T * d.E * 16 + T * d.k * 16 + U * (sizeof(moe::UnitDesc) + 32) + P * 8 + P * (d.I + d.H) * 4;
     if (cudaMemset(s.route_done, 0, 4) != cudaSuccess || cudaMemset(s.tile_done, 0, (d.H / 16) * 4) != cudaSuccess ||
@@ -446,13 +450,24 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, false); });
         timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });
         timed(h, 5, st, [&] { moe::launch_plan_prefill(d, h->scr, a, h->G, st); });
-        timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st, false); });
-        timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, bucket, st, false); });
         const int groups = (std::min(T * d.k, d.E) + h->G - 1) / h->G;
-        for (int g = 0; g < groups; ++g) {
-            timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
-            timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st, false); });
-            timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, bucket, st, false); });
+        if (moe::gemm_supported(d)) {
+            // tensor-core grouped GEMMs: resident units and the shared expert in
+            // place, then each staging group through the arena; one combine
+            timed(h, 2, st, [&] { moe::launch_gemm(d, h->scr, a.x, T, 1, 0, h->G, units, st); });
+            for (int g = 0; g < groups; ++g) {
+                timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
+                timed(h, 2, st, [&] { moe::launch_gemm(d, h->scr, a.x, T, 2, g, h->G, h->G, st); });
+            }
+            timed(h, 3, st, [&] { moe::launch_combine(d, h->scr, out, T, st); });
+        } else {
+            timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st, false); });
+            timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, bucket, st, false); });
+            for (int g = 0; g < groups; ++g) {
+                timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
+                timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st, false); });
+                timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, bucket, st, false); });
+            }
         }
     }
     cudaError_t e = cudaGetLastError();
@@ -483,6 +498,7 @@ moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out) {
     CK(h, cudaMemcpy(&derr, h->scr.err, sizeof derr, cudaMemcpyDeviceToHost));
     if (derr & 1u) return fail(h, MOE_ERR_TIMEOUT, "a grid barrier of the one-kernel decode path timed out");
     if (derr & 2u) return fail(h, MOE_ERR_TIMEOUT, "a weight-slot wait of the one-kernel decode path timed out");
+    if (derr & 4u) return fail(h, MOE_ERR_TIMEOUT, "a tensor-core wait of the prefill GEMM timed out");
     return MOE_OK;
 }
 

@@ -95,7 +95,10 @@ struct Scratch {
     unsigned long long* copy_t1;
     unsigned* tiles_done;   // row tiles combined by the down kernel (whole call)
     unsigned* grid_bar;     // arrival counter of the fused layer kernel's grid barriers
-    unsigned* err;          // sticky device error bits (1: a grid barrier timed out)
+    unsigned* err;          // sticky device error bits (1: a grid barrier timed out, 2: a weight-slot
+                            // wait timed out, 4: a prefill GEMM wait timed out)
+    int2* gemm_items;       // prefill GEMM work list: (unit, 128-pair tile)
+    int* gemm_count;        // its length
 };
 
 // Device cache state and constants of a handle.
@@ -268,6 +271,15 @@ bool launch_layer(const CacheDev& c, const Scratch& s, const RouteArgs& a, float
                   bool pdl);
 bool launch_down_rows(const CacheDev& c, const Scratch& s, float* out, int T, int units, int bucket, cudaStream_t st,
                       bool pdl);
+
+// Prefill expert FFN as tcgen05 grouped GEMMs (gemm.cu): whether the format
+// takes it, the work-list bound for P pairs over Y units, one launch over the
+// units of `kind`/`group` (work list, gate/up, down), and the final combine.
+bool gemm_supported(const CacheDev& c);
+size_t gemm_max_items(int P, int Y);
+void launch_gemm(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G, int Y,
+                 cudaStream_t st);
+void launch_combine(const CacheDev& c, const Scratch& s, float* out, int T, cudaStream_t st);
 
 // Host-side repack of canonical records into the slot layout (repack.cpp).
 void repack_record(int fmt, int H, int I, const uint8_t* canonical, uint8_t* slot, float* gscales3);
