@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
     ap.add_argument("--split", action="store_true", help="route, gate/up and down as three kernels per decode call")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()
 
 
@@ -450,7 +452,7 @@ def run_ours(args):
     if os.path.exists(tfile):
         try:
             tj = json.load(open(tfile))
-            if tj.get("workload") == w.name and tj.get("kernel") == "gateup":
+            if tj.get("workload") == w.name and tj.get("kernel") == ("layer" if ly_hit is not None else "gateup"):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
@@ -515,10 +517,120 @@ def run_ours(args):
     return 0
 
 
+def run_prefill(args):
+    """Prompt-sized calls: the prefill workload's prompt (T tokens) through
+    each layer, steps times. A call routes every token, reads the resident
+    experts in place, stages the others from the pinned store through the
+    arena in groups, and runs the expert FFN as tensor-core grouped GEMMs.
+    Reports prefill tok/s and the GEMM stage's TFLOP/s (events per stage, in
+    a profiled pass after the timed one)."""
+    import numpy as np
+    import torch
+    import synth
+    from paged_expert_cache_gb300 import build as cbuild
+    cbuild.build()
+    synth.build()
+    import paged_expert_cache_gb300 as pec
+    from synth.workloads import WORKLOADS, scaled
+    w = WORKLOADS[args.workload if args.workload != "qwen3_30b_a3b_q4_0" else "flash_next_prefill"]
+    if args.layers:
+        w = scaled(w, L=args.layers)
+    T = w.prompt_T
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
+                          slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
+                          max_tokens=T, device=0)
+    t_setup = time.perf_counter()
+    cache = pec.MoECache(cfg)
+    buf = None
+    for l in range(w.L):
+        buf = synth.expert_records(w.fmt, w.seed, l, 0, w.E, w.H, w.I, out=buf)
+        cache.load_experts(l, 0, buf)
+        if w.has_shared:
+            cache.load_shared(l, synth.expert_record(w.fmt, w.seed, l, -1, w.H, w.I))
+    routers = torch.stack([torch.from_numpy(synth.router_weights(w.seed, l, w.E, w.H).view(np.int16))
+                           for l in range(w.L)]).to(dev)
+    bias = torch.from_numpy(synth.zipf_bias(w.E)).to(dev) if w.bias else None
+    prompts = torch.stack([torch.from_numpy(synth.prompt(w.seed, l, T, w.H).view(np.int16))
+                           for l in range(w.L)]).to(dev)
+    out = torch.empty((T, w.H), dtype=torch.float32, device=dev)
+    # decode steps of batch 1 leave a working set resident, as after a chat turn
+    xs = [torch.from_numpy(synth.hidden_ar1(w.seed, l, 0, PRIME, w.H, w.rho).view(np.int16)).to(dev)
+          for l in range(w.L)]
+    dec_out = torch.empty((1, w.H), dtype=torch.float32, device=dev)
+    for s_ in range(PRIME):
+        for l in range(w.L):
+            cache.forward(xs[l][s_:s_ + 1], routers[l], l, dec_out, bias=bias, T=1)
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def prompt_pass():
+        for l in range(w.L):
+            cache.forward(prompts[l], routers[l], l, out, bias=bias, T=T)
+
+    for _ in range(args.warmup):
+        prompt_pass()
+    torch.cuda.synchronize()
+    s0 = cache.stats()["buckets"][2]
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        prompt_pass()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    s1 = cache.stats()["buckets"][2]
+    # stage times, one profiled pass
+    cache.profile_read()
+    cache.profile_enable(True)
+    prompt_pass()
+    prof = cache.profile_read()
+    cache.profile_enable(False)
+    calls = w.L
+    P = T * w.k + (T if w.has_shared else 0)
+    flops = 2.0 * P * 3 * w.H * w.I  # per layer call: gate, up and down over every (token, expert) pair
+    gemm_us = prof["gateup"]["ms"] * 1e3 / calls
+    tflops = flops / (gemm_us * 1e-6) / 1e12 if gemm_us else None
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    tpeak = peaks.get("bf16_tflops", 1900.0)
+    staged = s1["misses"] - s0["misses"]
+    hits = s1["hits"] - s0["hits"]
+    line = {
+        "metric": "MoE prefill tok/s (prompt through each layer) + grouped-GEMM TFLOP/s", "impl": "ours",
+        "value": args.steps * T / (ms / 1e3), "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 tcgen05 products, fp32 accumulate in tensor memory", "data": "synthetic",
+        "config": {"workload": w.name, "prompt_tokens": T, "layers": w.L, "experts": w.E, "top_k": w.k,
+                   "format": w.fmt, "prefill_group": 32, "priming_decode_steps": PRIME},
+        "per_layer_call_us": ms * 1e3 / (args.steps * calls),
+        "resident_experts_per_call": hits / max(1, args.steps * calls),
+        "staged_experts_per_call": staged / max(1, args.steps * calls),
+        "stage_us_per_call": {k: prof[k]["ms"] * 1e3 / calls for k in prof},
+        "gemm": {"kernels": "k_gemm_items + k_gemm_gateup + k_gemm_down (tcgen05.mma kind::f16, M=N=128)",
+                 "algorithmic_flops_per_call": flops, "us_per_call": gemm_us, "tflops": tflops,
+                 "peak_tflops": tpeak, "frac": tflops / tpeak if tflops else None,
+                 "peak_src": "measured cuBLAS bf16 burst (fp16 has the same dense rate)"},
+        "staging_gbs": (staged / args.steps) * cache.info()["slot_bytes"] / (prof["copy"]["ms"] * 1e-3) / 1e9
+        if prof["copy"]["ms"] else None,
+        "clocks": clk, "setup_s": setup_s,
+    }
+    print(json.dumps(line))
+    cache.close()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill:
+        return run_prefill(args)
     return run_ours(args)
 
 

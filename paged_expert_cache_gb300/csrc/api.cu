@@ -37,6 +37,7 @@ struct moe_cache {
     bool prof_on = false;
     bool fused_ok = true;  // the one-kernel decode path launched (or was not tried yet)
     uint64_t fused_calls = 0, split_calls = 0;
+    int last_layer = -1;    // layer of the previous layer call on this handle (-1: none since reset)
     std::vector<cudaEvent_t> ev_pool;
     size_t ev_used = 0;
     struct Span { int stage, a, b; };
@@ -391,6 +392,12 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     a.layer = layer_id;
     a.prefill = decode ? 0 : 1;
     a.bucket = bucket;
+    // Per-layer pools: this layer's state was last written by its own previous
+    // call. When the call just before this one on the handle was another
+    // layer's, that write belongs to a grid at least two back in stream order,
+    // which has completed by the time this call's kernel can start.
+    a.early = (d.pool_mode == 0 && h->last_layer >= 0 && h->last_layer != layer_id) ? 1 : 0;
+    h->last_layer = layer_id;
     const int units = std::min(T * d.k, d.E) + d.has_shared;
     // programmatic dependent launch between the decode kernels (off while
     // events bracket each launch for profiling)
@@ -631,6 +638,7 @@ moe_status_t moe_cache_reset(moe_cache_t* h) {
     if (!h) return fail(nullptr, MOE_ERR_INVALID, "handle is NULL");
     CK(h, cudaSetDevice(h->cfg.device));
     CK(h, cudaDeviceSynchronize());
+    h->last_layer = -1;
     return init_tables(h);
 }
 

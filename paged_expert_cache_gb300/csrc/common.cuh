@@ -233,6 +233,8 @@ struct RouteArgs {
     const uint16_t* w;   // [E][H] bf16
     const float* bias;   // [E] or null
     int T, layer, prefill, bucket;
+    int early;           // 1: no call still in flight can write this layer's pool state, so a decode
+                         // kernel may read it before waiting on the preceding grid
 };
 
 void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st, bool pdl);

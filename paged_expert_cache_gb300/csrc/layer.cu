@@ -412,19 +412,36 @@ __device__ __forceinline__ void drain_ring(const LayerLayout& L, uint8_t* smem, 
 }
 
 
-// Gate/up of one 16-row tile of a missed unit, read from the mapped host store
-// (Wg: gate; up follows at the matrix stride) and written through to its slot
-// (Dg) as it is read, by one group of eight warps (gw: the warp in the group,
-// gtid: the thread). Out of line: calls with misses are bound by the host
-// link, and the all-hit path keeps a short instruction stream.
+// One gate/up item (16-row tile rt) of a missed unit, read from the mapped
+// host store over the host link (Wg: gate; up follows at the matrix stride)
+// and written through to its slot (Dg) as it is read, by one group of eight
+// warps (gw: the warp in the group, gtid: the thread); plus the item's share
+// of the record's down matrix, copied to the slot, so the whole record crosses
+// the link in this pass. All of a thread's loads for the gate/up chunks and
+// the first batch of its down share are in flight at once: the link's latency
+// is paid about once per item. Out of line: calls with misses are bound by
+// the host link, and the all-hit path keeps a short instruction stream.
 template <int FMT>
-__device__ __noinline__ void gateup_pull(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
-                                         int lane, const uint16_t* brow, float (&ag)[4], float (&au)[4]) {
-    constexpr int CIF = FMT == FMT_BF16 ? 1 : 2;  // chunks in flight
+__device__ __noinline__ void pull_item(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
+                                       int lane, const uint16_t* brow, float (&ag)[4], float (&au)[4]) {
+    constexpr bool kNib = FMT == FMT_Q4_0 || FMT == FMT_NVFP4;
+    constexpr int CIF = kNib ? 4 : (FMT == FMT_FP8_B128 ? 2 : 1);  // chunks in flight per matrix
+    constexpr int DS = kNib ? 2 : (FMT == FMT_FP8_B128 ? 2 : 1);    // down-share vectors in flight
     const uint64_t mgu = matrix_stride(FMT, I, H);
     const uint8_t* Wu = Wg + mgu;
     uint8_t* Du = Dg + mgu;
-    const int KC = H / 64, cpw = (KC + 7) / 8;
+    const int KC = H / 64, cpw = (KC + 7) / 8, RT = I / 16;
+    // this item's share of the down matrix
+    const uint64_t nvec = matrix_stride(FMT, H, I) / 16, per = (nvec + RT - 1) / RT;
+    const uint64_t v0 = (uint64_t)rt * per, v1 = v0 + per < nvec ? v0 + per : nvec;
+    const uint8_t* src = Wg + 2 * mgu;
+    uint8_t* dst = Dg + 2 * mgu;
+    uint4 dbuf[DS];
+#pragma unroll
+    for (int i = 0; i < DS; ++i) {
+        const uint64_t vi = v0 + gtid + (uint64_t)i * 256;
+        if (vi < v1) dbuf[i] = ldg_stream(src + vi * 16);
+    }
     if (rt == 0) {
         copy_matrix_tail<FMT>(Wg, Dg, I, H, gtid, 256);
         copy_matrix_tail<FMT>(Wu, Du, I, H, gtid, 256);
@@ -450,22 +467,14 @@ __device__ __noinline__ void gateup_pull(const uint8_t* Wg, uint8_t* Dg, int I, 
             }
         }
     }
-}
-
-// Row tile rt's share of a missed record's down matrix, copied from the host
-// store to the slot by one group (256 threads), so the whole record crosses
-// the host link in the gate/up pass.
-template <int FMT>
-__device__ __noinline__ void pull_down_share(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid) {
-    const uint64_t mgu = matrix_stride(FMT, I, H);
-    const int RT = I / 16;
-    const uint64_t mdn = matrix_stride(FMT, H, I);
-    const uint64_t nvec = mdn / 16, per = (nvec + RT - 1) / RT;
-    const uint64_t v0 = (uint64_t)rt * per, v1 = v0 + per < nvec ? v0 + per : nvec;
-    const uint8_t* src = Wg + 2 * mgu;
-    uint8_t* dst = Dg + 2 * mgu;
+#pragma unroll
+    for (int i = 0; i < DS; ++i) {
+        const uint64_t vi = v0 + gtid + (uint64_t)i * 256;
+        if (vi < v1) stg_stream(dst + vi * 16, dbuf[i]);
+    }
+    // the rest of the share, if the item's share is larger than one batch
     constexpr int kBatch = 4;
-    for (uint64_t v = v0 + gtid; v < v1; v += 256ull * kBatch) {
+    for (uint64_t v = v0 + (uint64_t)DS * 256 + gtid; v < v1; v += 256ull * kBatch) {
         uint4 buf[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
@@ -517,35 +526,38 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     if (e_mine < E)
         for (int i = 0; i < H / 256; ++i)
             cp_async16(wr + lane * 8 + i * 256, a.w + (size_t)e_mine * H + lane * 8 + i * 256);
-    griddep_wait();
-    griddep_launch();
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
     const PlanSmem m = plan_layout(smem + L.plan, E, c.K, n_ids, U, P);
-    unsigned phase = 0;
-    {
-        // one round of asynchronous copies: the tokens and the pool's state
-        // (stamps, keys, the layer's slot map, NVFP4 global scales), read by
-        // every CTA before the first barrier (only the committing CTA writes
-        // them, after)
+    // the pool's state (stamps, keys, the layer's slot map, its clock, NVFP4
+    // global scales): read by every CTA before the first barrier, written
+    // only by the committing CTA after it; read before the wait on the
+    // preceding grid when that grid cannot be writing it
+    auto stage_state = [&]() {
         const unsigned long long* lu = c.last_use + (size_t)pool * c.K;
         const int* kof = c.key_of + (size_t)pool * c.K;
         const int* smap = c.slot_map + (size_t)a.layer * E;
-        for (int i = tid; i < T * (H / 8); i += kLThreads) cp_async16(xs + (size_t)i * 8, a.x + (size_t)i * 8);
         for (int i = tid; i < c.K; i += kLThreads) {
             cp_async8(m.lu + i, lu + i);
             cp_async4(m.kof + i, kof + i);
         }
-        for (int i = tid; i < E; i += kLThreads) {
-            cp_async4(m.smap + i, smap + i);
-            m.first[i] = 0x7fffffff;
-        }
+        for (int i = tid; i < E; i += kLThreads) cp_async4(m.smap + i, smap + i);
         if (c.fmt == FMT_NVFP4) {
             for (int i = tid; i < E * 3; i += kLThreads) cp_async4(m.gl + i, c.gtable + (size_t)a.layer * E * 3 + i);
             if (tid < 3) cp_async4(m.gl + E * 3 + tid, c.gtable + ((size_t)c.L * E + a.layer) * 3 + tid);
         }
+        if (tid == 0) clk = c.clock[pool];
+    };
+    if (a.early) stage_state();
+    griddep_wait();
+    griddep_launch();
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
+    unsigned phase = 0;
+    {
+        // the tokens, and the pool's state if not staged yet
+        for (int i = tid; i < T * (H / 8); i += kLThreads) cp_async16(xs + (size_t)i * 8, a.x + (size_t)i * 8);
+        if (!a.early) stage_state();
+        for (int i = tid; i < E; i += kLThreads) m.first[i] = 0x7fffffff;
         for (int i = tid; i <= E / 32; i += kLThreads) m.missbits[i] = 0u;
         if (tid == 0) {
-            clk = c.clock[pool];
             rerank = 0;
             unsigned cur;
             asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(cur) : "l"(s.grid_bar) : "memory");
@@ -646,10 +658,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     const uint64_t mgu = matrix_stride(FMT, I, H);
     const Pieces q = make_pieces(b, G, RT, RTD, n_units, L.m);
     const uint64_t pol = policy_evict_first();
-    if (tid == 0) {
-        // the ring reuses shared memory the generic proxy wrote in phases 1-2
+    if (lane == 0 && warp < q.n && warp < L.ns) {
+        // lane 0 of warp w issues piece w, so the first pieces of both groups
+        // are requested at once; the ring reuses shared memory the generic
+        // proxy wrote in phases 1-2
         fence_proxy_async();
-        for (int i = 0; i < q.n && i < L.ns; ++i) issue_piece<FMT>(i, q, L, sd, smem, H, I, pol);
+        issue_piece<FMT>(warp, q, L, sd, smem, H, I, pol);
     }
     const uint8_t* ring = smem + L.ring;
     {
@@ -664,7 +678,6 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             const UnitDesc d = sd[u];
             const int slot = j % L.ns;
             const uint8_t* Wg = reinterpret_cast<const uint8_t*>(d.src);
-            const uint8_t* Wu = Wg + mgu;
             uint8_t* Dg = d.dst ? reinterpret_cast<uint8_t*>(d.dst) : nullptr;
             const int np = d.np;
             // this lane's token row of the B tile (zero row past the unit's pairs)
@@ -694,7 +707,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
                 // missed: read the tile from the mapped host store over the
                 // host link and write it through to the slot
                 if (gtid == 0) atomicMin(s.copy_t0, globaltimer_ns());
-                gateup_pull<FMT>(Wg, Dg, I, H, rt, gtid, gw, lane, brow, ag, au);
+                pull_item<FMT>(Wg, Dg, I, H, rt, gtid, gw, lane, brow, ag, au);
             }
             const int g = lane >> 2, qd = lane & 3;
             float* rg = red + (size_t)(gw * 2) * 128;
@@ -723,11 +736,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
                     s.act[(size_t)pair * I + rt * 16 + row] = silu_f(gs * d.g[0]) * (us * d.g[1]);
                 }
             }
-            if (Dg) {
-                // this item's share of the missed record's down matrix
-                pull_down_share<FMT>(Wg, Dg, I, H, rt, gtid);
-                if (gtid == 0) atomicMax(s.copy_t1, globaltimer_ns());
-            }
+            if (Dg && gtid == 0) atomicMax(s.copy_t1, globaltimer_ns());
             group_sync(grp);
         }
     }

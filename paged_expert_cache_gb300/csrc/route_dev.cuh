@@ -488,11 +488,18 @@ static __device__ __forceinline__ void topk_token_fast(const CacheDev& c, const 
     sort_desc<NPL>(key);
     __syncwarp();
     for (int j = 0; j < k; ++j) {
-        unsigned long long best = key[0];
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
+        // the largest head over the lanes: its high word by one reduction,
+        // then (when heads tie there) its low word among the tied lanes; the
+        // keys are distinct, so one lane holds the winner
+        const unsigned hi = (unsigned)(key[0] >> 32);
+        const unsigned mhi = __reduce_max_sync(0xffffffffu, hi);
+        const unsigned tied = __ballot_sync(0xffffffffu, hi == mhi);
+        unsigned long long best;
+        if (__popc(tied) == 1) {
+            best = __shfl_sync(0xffffffffu, key[0], __ffs(tied) - 1);
+        } else {
+            const unsigned lo = hi == mhi ? (unsigned)key[0] : 0u;
+            best = ((unsigned long long)mhi << 32) | __reduce_max_sync(0xffffffffu, lo);
         }
         if (key[0] == best) {
             const int e = 1023 - (int)(best & 1023ull);
