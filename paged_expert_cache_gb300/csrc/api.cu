@@ -40,6 +40,10 @@ struct moe_cache {
     int last_layer = -1;    // layer of the previous layer call on this handle (-1: none since reset)
     std::vector<cudaEvent_t> ev_pool;
     size_t ev_used = 0;
+    // prefill staging: a side stream copies group g + 1 into one half of the
+    // arena while the tensor-core GEMMs of group g read the other half
+    cudaStream_t stage_stream = nullptr;
+    cudaEvent_t ev_plan = nullptr, ev_copy[2] = {nullptr, nullptr}, ev_gemm[2] = {nullptr, nullptr};
     struct Span { int stage, a, b; };
     std::vector<Span> spans;
 };
@@ -96,6 +100,12 @@ void timed(moe_cache_t* h, int stage, cudaStream_t st, F&& launch) {
 void free_all(moe_cache_t* h) {
     for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
     h->ev_pool.clear();
+    for (cudaEvent_t* e : {&h->ev_plan, &h->ev_copy[0], &h->ev_copy[1], &h->ev_gemm[0], &h->ev_gemm[1]}) {
+        if (*e) cudaEventDestroy(*e);
+        *e = nullptr;
+    }
+    if (h->stage_stream) cudaStreamDestroy(h->stage_stream);
+    h->stage_stream = nullptr;
     for (void* p : h->dev_allocs) cudaFree(p);
     h->dev_allocs.clear();
     if (h->store_host) cudaFreeHost(h->store_host);
@@ -286,6 +296,11 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     if (h->maxT > c.max_cache_tokens) {
         DA(s.gemm_items, moe::gemm_max_items(P, U));
         DA(s.gemm_count, 1);
+        if (cudaStreamCreateWithFlags(&h->stage_stream, cudaStreamNonBlocking) != cudaSuccess)
+            return bail(MOE_ERR_CUDA, "staging stream creation failed");
+        for (cudaEvent_t* ev : {&h->ev_plan, &h->ev_copy[0], &h->ev_copy[1], &h->ev_gemm[0], &h->ev_gemm[1]})
+            if (cudaEventCreateWithFlags(ev, cudaEventDisableTiming) != cudaSuccess)
+                return bail(MOE_ERR_CUDA, "staging event creation failed");
     }
 #undef DA
     h->scratch_bytes = T * d.E * 16 + T * d.k * 16 + U * (sizeof(moe::UnitDesc) + 32) + P * 8 + P * (d.I + d.H) * 4;
@@ -460,18 +475,29 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         const int groups = (std::min(T * d.k, d.E) + h->G - 1) / h->G;
         if (moe::gemm_supported(d)) {
             // tensor-core grouped GEMMs: resident units and the shared expert in
-            // place, then each staging group through the arena; one combine
+            // place, then each staging group through the arena; one combine.
+            // Group g + 1 is staged over the host link on the side stream into
+            // the arena half group g - 1 used, while the GEMMs of group g run:
+            // events order each copy after the GEMMs that last read its half
+            // and each group's GEMMs after its copy.
+            cudaStream_t cs = h->stage_stream;
+            CK(h, cudaEventRecord(h->ev_plan, st));
+            CK(h, cudaStreamWaitEvent(cs, h->ev_plan, 0));
             timed(h, 2, st, [&] { moe::launch_gemm(d, h->scr, a.x, T, 1, 0, h->G, units, st); });
             for (int g = 0; g < groups; ++g) {
-                timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
+                if (g >= 2) CK(h, cudaStreamWaitEvent(cs, h->ev_gemm[g & 1], 0));
+                timed(h, 1, cs, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, cs, true); });
+                CK(h, cudaEventRecord(h->ev_copy[g & 1], cs));
+                CK(h, cudaStreamWaitEvent(st, h->ev_copy[g & 1], 0));
                 timed(h, 2, st, [&] { moe::launch_gemm(d, h->scr, a.x, T, 2, g, h->G, h->G, st); });
+                CK(h, cudaEventRecord(h->ev_gemm[g & 1], st));
             }
             timed(h, 3, st, [&] { moe::launch_combine(d, h->scr, out, T, st); });
         } else {
             timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 1, 0, h->G, units, st, false); });
             timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 1, 0, h->G, units, bucket, st, false); });
             for (int g = 0; g < groups; ++g) {
-                timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st); });
+                timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st, false); });
                 timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st, false); });
                 timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, bucket, st, false); });
             }

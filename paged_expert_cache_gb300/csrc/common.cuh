@@ -240,7 +240,8 @@ struct RouteArgs {
 void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st, bool pdl);
 void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
 void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st);
-void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st);
+void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st,
+                 bool beside_compute);
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
                    int units, cudaStream_t st, bool pdl);
 void launch_down(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,

@@ -389,14 +389,18 @@ __global__ void __launch_bounds__(kCopyThreads) k_copy(CacheDev c, Scratch s, in
 // ---------------------------------------------------------------------------
 static int g_copy_ctas = 0;
 
-void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st) {
+void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st,
+                 bool beside_compute) {
     if (!g_copy_ctas) {
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        g_copy_ctas = 2 * (sms > 0 ? sms : 148);
+        g_copy_ctas = sms > 0 ? sms : 148;
     }
-    k_copy<<<g_copy_ctas, kCopyThreads, 0, st>>>(c, s, first, count, bucket);
+    // alone: two CTAs per SM; beside the GEMMs of another group: a quarter of
+    // the SMs, whose loads in flight (~1 MB) still cover the host link
+    const int ctas = beside_compute ? (g_copy_ctas + 3) / 4 : 2 * g_copy_ctas;
+    k_copy<<<ctas, kCopyThreads, 0, st>>>(c, s, first, count, bucket);
 }
 
 template <int FMT>
