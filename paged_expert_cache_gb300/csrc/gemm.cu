@@ -285,37 +285,49 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
     const uint8_t* Wu = Wg + mgu;
     constexpr uint32_t idesc = tc_idesc_f16(kGM, kGN);
     bool ok = true;
+    // Software pipeline: the global loads of chunk kc + 1 (weight fragments
+    // and token rows) are issued before chunk kc is dequantised and stored,
+    // so their latency overlaps the stores, the barrier and the MMA issue.
+    // warp w dequantises row tile w of the gate and up tiles; thread i stages
+    // token rows j = i / 8 + 32 r, 16-byte column chunk i % 8, r = 0..3
+    constexpr int kTokPerThread = kGN * 8 / kGThreads;
+    const int rt = m * (kGM / 16) + warp;
+    Chunk<FMT> cg, cu;
+    uint4 xv[kTokPerThread];
+    auto load_next = [&](int kc) {
+        load_chunk<FMT>(Wg, nullptr, I, H, rt, kc, lane, cg);
+        load_chunk<FMT>(Wu, nullptr, I, H, rt, kc, lane, cu);
+#pragma unroll
+        for (int r = 0; r < kTokPerThread; ++r) {
+            const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
+            xv[r] = tok[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok[j] * H + kc * 64 + cc * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    load_next(0);
     for (int kc = 0; kc < KC; ++kc) {
         const int st = kc & 1;
         uint8_t* stage = sm + (size_t)st * kGStage;
         // the MMAs of chunk kc - 2 read this stage
         if (kc >= kGStages && !gbar_wait(gsmem(&bars[st]), (uint32_t)(((kc - kGStages) / kGStages) & 1))) ok = false;
         {
-            // weights: warp w dequantises row tile w of the gate and up tiles
-            const int rt = m * (kGM / 16) + warp;
-            Chunk<FMT> cg, cu;
-            load_chunk<FMT>(Wg, nullptr, I, H, rt, kc, lane, cg);
-            load_chunk<FMT>(Wu, nullptr, I, H, rt, kc, lane, cu);
             uint32_t a[4][4];
             frag_to_f16<FMT>(cg, a);
             store_frag(stage, warp, lane, a);
             frag_to_f16<FMT>(cu, a);
             store_frag(stage + kGTile, warp, lane, a);
         }
-        // tokens: pair row j, 16-byte column chunk cc, bf16 -> fp16
-        for (int i = tid; i < kGN * 8; i += kGThreads) {
-            const int j = i >> 3, cc = i & 7;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok[j] >= 0) {
-                v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok[j] * H + kc * 64 + cc * 8));
-                uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        // tokens: bf16 -> fp16 (bf16 values are exact in fp16)
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    w4[q] = h2_as_u32(__floats2half2_rn(__uint_as_float(w4[q] << 16), __uint_as_float(w4[q] & 0xffff0000u)));
-                v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-            *reinterpret_cast<uint4*>(stage + 2 * kGTile + sw128(j, cc * 8)) = v;
+        for (int r = 0; r < kTokPerThread; ++r) {
+            const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
+            uint32_t w4[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w4[q] = h2_as_u32(__floats2half2_rn(__uint_as_float(w4[q] << 16), __uint_as_float(w4[q] & 0xffff0000u)));
+            *reinterpret_cast<uint4*>(stage + 2 * kGTile + sw128(j, cc * 8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+        if (kc + 1 < KC) load_next(kc + 1);
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -404,25 +416,43 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
     const uint8_t* Wd = reinterpret_cast<const uint8_t*>(d.src) + 2 * matrix_stride(FMT, I, H);
     constexpr uint32_t idesc = tc_idesc_f16(kGM, kGN);
     bool ok = true;
+    // the same software pipeline as gate/up: chunk kc + 1's weight fragments
+    // and activations are in flight while chunk kc is staged
+    constexpr int kActPerThread = kGN * 8 / kGThreads;
+    const int rt = m * (kGM / 16) + warp;
+    Chunk<FMT> ch;
+    float4 av[kActPerThread][2];
+    auto load_next = [&](int kc) {
+        load_chunk<FMT>(Wd, nullptr, H, I, rt, kc, lane, ch);
+#pragma unroll
+        for (int r = 0; r < kActPerThread; ++r) {
+            const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
+            if (pairs[j] >= 0) {
+                const float4* src = reinterpret_cast<const float4*>(s.act + (size_t)pairs[j] * I + kc * 64 + cc * 8);
+                av[r][0] = __ldcg(src);
+                av[r][1] = __ldcg(src + 1);
+            } else {
+                av[r][0] = av[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    load_next(0);
     for (int kc = 0; kc < KC; ++kc) {
         const int st = kc & 1;
         uint8_t* stage = sm + (size_t)st * kGStage;
         if (kc >= kGStages && !gbar_wait(gsmem(&bars[st]), (uint32_t)(((kc - kGStages) / kGStages) & 1))) ok = false;
         {
-            const int rt = m * (kGM / 16) + warp;
-            Chunk<FMT> ch;
-            load_chunk<FMT>(Wd, nullptr, H, I, rt, kc, lane, ch);
             uint32_t a[4][4];
             frag_to_f16<FMT>(ch, a);
             store_frag(stage, warp, lane, a);
         }
         // activations of the pairs: fp32 -> fp16 hi (tile 2) + lo (tile 1)
-        for (int i = tid; i < kGN * 8; i += kGThreads) {
-            const int j = i >> 3, cc = i & 7;
+#pragma unroll
+        for (int r = 0; r < kActPerThread; ++r) {
+            const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
             uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
-            if (pairs[j] >= 0) {
-                const float4* src = reinterpret_cast<const float4*>(s.act + (size_t)pairs[j] * I + kc * 64 + cc * 8);
-                const float4 f0 = __ldcg(src), f1 = __ldcg(src + 1);
+            {
+                const float4 f0 = av[r][0], f1 = av[r][1];
                 const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
                 uint32_t h[4], l[4];
 #pragma unroll
@@ -439,6 +469,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
             *reinterpret_cast<uint4*>(stage + 2 * kGTile + sw128(j, cc * 8)) = hv;
             *reinterpret_cast<uint4*>(stage + kGTile + sw128(j, cc * 8)) = lv;
         }
+        if (kc + 1 < KC) load_next(kc + 1);
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
