@@ -189,7 +189,13 @@ moe_status_t moe_cache_load_shared(moe_cache_t* h, int32_t layer, const void* re
  * reads resident experts in place without changing the LRU order and stages
  * the others through a double-buffered arena in groups of prefill_group
  * [T4, "What the MoE Cache Actually Caches"; NVME, "Workflow"; FP4LOCAL,
- * "Prefill"]. Errors (nothing is enqueued and the state is untouched):
+ * "Prefill"]. For Q4_0, block-FP8 and NVFP4 experts the prefill FFN runs as
+ * tensor-core grouped GEMMs with fp16 operands (Q4_0 and block-FP8 weights
+ * are rounded to fp16 there; NVFP4 weights are exact) and the staging copies
+ * run on an internal side stream beside them; every kernel of the call that
+ * reads a staged group waits for its copy on `stream`, so work issued on
+ * `stream` after the call is ordered after all of it.
+ * Errors (nothing is enqueued and the state is untouched):
  * MOE_ERR_INVALID for a bad layer, T <= 0 or T > max_tokens, null pointers;
  * MOE_ERR_CAPACITY when T * top_k exceeds the layer's pool on the decode path
  * (the single-wave rule of [PAGED, "What happens with more than one
