@@ -82,7 +82,7 @@ __host__ __device__ inline size_t tile_bytes_bound(int fmt, int C) {
 //   region B:   gate/up partial tiles  |  down staging (activations, partials)
 struct LayerLayout {
     size_t sd, ids, wts, xg, bars, last;
-    size_t xs, wr, plan, topk;
+    size_t xs, wr, plan, topk, rk;
     size_t ring;
     size_t red, ah, al, ps;
     size_t gl;       // offset of the up matrix in a gate/up piece (bound of one tile)
@@ -111,6 +111,7 @@ __host__ __device__ inline LayerLayout layer_layout(int fmt, int E, int K, int k
     L.wr = p; p = align16(p + (size_t)rows * H * 2);
     L.plan = p; p = align16(p + plan_layout(nullptr, E, K, n_ids, U, P).bytes);
     L.topk = p; p = align16(p + (size_t)(T < kLayerRankWarps ? T : kLayerRankWarps) * topk_bytes_per_warp(E));
+    L.rk = p; p = align16(p + (size_t)E * 8 + (size_t)kLWarps * 8);  // rank keys, per-warp bounds (one token)
     const size_t phase12 = p - a0;
     // region B: gate/up partials, or the down staging
     const size_t ld = (size_t)I + 8;
@@ -588,7 +589,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     if (!grid_barrier(s.grid_bar, s.err, phase)) return;  // nothing is in flight yet
 
     // ---- 2. top-k and plan in every CTA ----------------------------------
-    {
+    if (T == 1 && E <= 256) {
+        // one token: every expert ranked at once by its own thread
+        const TopkSmem tw = topk_layout(smem + L.topk, E);
+        topk_rank_block(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
+                        reinterpret_cast<float2*>(smem + L.rk + (size_t)E * 8), &rerank, sids, swts);
+    } else {
         const int nrw = min(T, kLayerRankWarps);
         if (warp < nrw) {
             const TopkSmem tw = topk_layout(smem + L.topk + (size_t)warp * topk_bytes_per_warp(E), E);
@@ -596,7 +602,13 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         }
     }
     __syncthreads();
+    // The last CTA commits the call's cache transaction. When it owns no output
+    // row tile it commits after the second barrier, off the critical path: it
+    // takes the same descriptors as the others before, and runs the full plan
+    // on a fresh copy of the pool's state after (nothing else writes that state
+    // during the call, and every CTA read it before the first barrier).
     const bool commit = b == G - 1;
+    const bool defer = commit && b >= H / 16;
     if (commit) {
         for (int i = tid; i < n_ids; i += kLThreads) {
             s.ids[i] = sids[i];
@@ -614,7 +626,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     __shared__ int fast;
     if (warp == 0) {
         int ok = 0;
-        if (T == 1 && !commit) {
+        if (T == 1 && (!commit || defer)) {
             const int sl = lane < k ? m.smap[sids[lane]] : 0;
             ok = __all_sync(0xffffffffu, sl >= 0);
             if (ok && lane <= k) {
@@ -648,7 +660,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     if (fast) {
         n_units = k + (c.has_shared ? 1 : 0);
     } else {
-        plan_small(c, s, a, m, clk, sids, sd, commit);
+        plan_small(c, s, a, m, clk, sids, sd, commit && !defer);
         n_units = m.scal[0] + (c.has_shared ? 1 : 0);
     }
     __syncthreads();  // the ring below overlaps the plan's shared memory
@@ -747,6 +759,15 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     }
 
     // ---- 4. down projection + combine by row tiles -------------------------
+    if (defer) {
+        // this CTA has no row tile: its ring and staging are free for the plan
+        stage_state();
+        for (int i = tid; i < E; i += kLThreads) m.first[i] = 0x7fffffff;
+        for (int i = tid; i <= E / 32; i += kLThreads) m.missbits[i] = 0u;
+        cp_async_wait();
+        __syncthreads();
+        plan_small(c, s, a, m, clk, sids, sd, true);
+    }
     if (commit && tid == 0) {
         // every miss of the call has been streamed: book the time
         const unsigned long long t1 = atomicAdd(s.copy_t1, 0ull);

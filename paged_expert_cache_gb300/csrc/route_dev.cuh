@@ -454,6 +454,60 @@ __device__ __forceinline__ void sort_desc(unsigned long long (&key)[NPL]) {
     }
 }
 
+// Certifies the k picks in w.sel / w.selz / w.selb (rank order) against
+// their bounds, given mx, the largest upper bound (z + b, as a pair) over the
+// experts not picked, and writes the token's ids and weights; where the bounds
+// leave the order open, ranks the token again exactly (topk_token). One warp.
+static __device__ void topk_certify_finish(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
+                                           const TopkSmem& w, float2 mx, int* rerank_flag, int* ids_out,
+                                           float* wts_out) {
+    const int E = c.E, k = c.k, lane = threadIdx.x & 31;
+    // certify: lane j checks that pick j's lower bound is above the upper
+    // bounds of every later pick and of every expert not picked
+    float2 lower = make_float2(-INFINITY, 0.f), sfx = make_float2(-INFINITY, 0.f);
+    if (lane < k) {
+        const float2 zj = w.selz[lane];
+        const float bj = w.selb[lane];
+        lower = norm_pair(zj.x, __fsub_rd(zj.y, bj));
+        sfx = norm_pair(zj.x, __fadd_ru(zj.y, bj));
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {  // inclusive suffix max over lanes lane..31
+        const float2 o = make_float2(__shfl_down_sync(0xffffffffu, sfx.x, off), __shfl_down_sync(0xffffffffu, sfx.y, off));
+        if (lane + off < 32 && pair_gt(o, sfx)) sfx = o;
+    }
+    float2 later = make_float2(__shfl_down_sync(0xffffffffu, sfx.x, 1), __shfl_down_sync(0xffffffffu, sfx.y, 1));
+    if (lane == 31 || lane + 1 >= k) later = make_float2(-INFINITY, 0.f);
+    if (pair_gt(mx, later)) later = mx;
+    const bool ok = __all_sync(0xffffffffu, lane >= k || pair_gt(lower, later));
+    if (!ok) {
+        topk_token(c, s, a, t, w, rerank_flag, ids_out, wts_out);
+        return;
+    }
+    float zref = -INFINITY, sum = 0.f;
+    if (!c.norm_topk) {
+        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    } else {
+        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
+        zref = zj;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        sum = lane < k ? expf(zj - zref) : 0.f;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
+    if (lane < k) {
+        ids_out[t * k + lane] = w.sel[lane];
+        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
+    }
+    __syncwarp();
+}
+
 // Top-k of token t by one warp, from sorted per-lane lists. Lane l holds the
 // experts l, l + 32, ... as 64-bit keys: ord(hi) in the high word, then ord(lo)
 // with its low ten bits replaced by 1023 - e, so keys are distinct and order
@@ -527,58 +581,69 @@ static __device__ __forceinline__ void topk_token_fast(const CacheDev& c, const 
         const float2 o = shfl_pair(mx, off);
         if (pair_gt(o, mx)) mx = o;
     }
-    // certify: lane j checks that pick j's lower bound is above the upper
-    // bounds of every later pick and of every expert not picked
-    float2 lower = make_float2(-INFINITY, 0.f), sfx = make_float2(-INFINITY, 0.f);
-    if (lane < k) {
-        const float2 zj = w.selz[lane];
-        const float bj = w.selb[lane];
-        lower = norm_pair(zj.x, __fsub_rd(zj.y, bj));
-        sfx = norm_pair(zj.x, __fadd_ru(zj.y, bj));
+    topk_certify_finish(c, s, a, t, w, mx, rerank_flag, ids_out, wts_out);
+}
+
+
+// Top-k of token 0 by the first E threads of the CTA (E <= blockDim.x): thread
+// e builds expert e's key (the orderable 64-bit key of topk_token_fast: the
+// logit's high part, then its low part with 1023 - e in the low bits, so keys
+// are distinct), and its rank is the number of keys above it. Ranks below k
+// are the picks, in the same order as the sorted-list rounds give; the largest
+// upper bound over the rest comes from a block reduction. Warp 0 then
+// certifies and weighs as topk_token_fast does. Every thread of the CTA
+// calls it; keys: E entries and ub: blockDim.x / 32 entries of shared memory.
+static __device__ void topk_rank_block(const CacheDev& c, const Scratch& s, const RouteArgs& a, const TopkSmem& w,
+                                       unsigned long long* keys, float2* ub, int* rerank_flag, int* ids_out,
+                                       float* wts_out) {
+    const int E = c.E, k = c.k, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float2 z = make_float2(-INFINITY, 0.f);
+    float bd = 0.f;
+    unsigned long long key = 0ull;
+    if (tid < E) {
+        z = __ldcg(s.logits + tid);
+        bd = __ldcg(s.bounds + tid);
+        w.z[tid] = z;
+        w.b[tid] = bd;
+        key = ((unsigned long long)ord32(z.x) << 32) |
+              (unsigned long long)((ord32(__fadd_rn(z.y, 0.0f)) & ~1023u) | (unsigned)(1023 - tid));
+        keys[tid] = key;
     }
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {  // inclusive suffix max over lanes lane..31
-        const float2 o = make_float2(__shfl_down_sync(0xffffffffu, sfx.x, off), __shfl_down_sync(0xffffffffu, sfx.y, off));
-        if (lane + off < 32 && pair_gt(o, sfx)) sfx = o;
-    }
-    float2 later = make_float2(__shfl_down_sync(0xffffffffu, sfx.x, 1), __shfl_down_sync(0xffffffffu, sfx.y, 1));
-    if (lane == 31 || lane + 1 >= k) later = make_float2(-INFINITY, 0.f);
-    if (pair_gt(mx, later)) later = mx;
-    const bool ok = __all_sync(0xffffffffu, lane >= k || pair_gt(lower, later));
-    if (!ok) {
-        topk_token(c, s, a, t, w, rerank_flag, ids_out, wts_out);
-        return;
-    }
-    float zref = -INFINITY, sum = 0.f;
-    if (!c.norm_topk) {
-#pragma unroll
-        for (int m = 0; m < NPL; ++m) {
-            const int e = lane + 32 * m;
-            if (e < E) zref = fmaxf(zref, wz[e].x);
+    __syncthreads();
+    float2 up = make_float2(-INFINITY, 0.f);
+    if (tid < E) {
+        int rank = 0;
+        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
+#pragma unroll 4
+        for (int i = 0; i < E / 2; ++i) {
+            const ulonglong2 v = k2[i];
+            rank += (v.x > key) + (v.y > key);
         }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-#pragma unroll
-        for (int m = 0; m < NPL; ++m) {
-            const int e = lane + 32 * m;
-            if (e < E) sum += expf(wz[e].x - zref);
+        if (E & 1) rank += keys[E - 1] > key;
+        if (rank < k) {
+            w.sel[rank] = tid;
+            w.selz[rank] = z;
+            w.selb[rank] = bd;
+        } else {
+            up = norm_pair(z.x, __fadd_ru(z.y, bd));
         }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    } else {
-        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
-        zref = zj;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        sum = lane < k ? expf(zj - zref) : 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     }
-    if (lane < k) {
-        ids_out[t * k + lane] = w.sel[lane];
-        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        const float2 o = shfl_pair(up, off);
+        if (pair_gt(o, up)) up = o;
     }
-    __syncwarp();
+    if (lane == 0) ub[warp] = up;
+    __syncthreads();
+    if (warp == 0) {
+        float2 mx = lane < (int)(blockDim.x >> 5) ? ub[lane] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float2 o = shfl_pair(mx, off);
+            if (pair_gt(o, mx)) mx = o;
+        }
+        topk_certify_finish(c, s, a, 0, w, mx, rerank_flag, ids_out, wts_out);
+    }
 }
 
 __device__ __forceinline__ void topk_dispatch(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
