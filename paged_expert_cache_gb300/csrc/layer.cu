@@ -400,6 +400,26 @@ __device__ __noinline__ void issue_piece(int i, const Pieces& q, const LayerLayo
     }
 }
 
+// Waits for piece i in its slot: first until the piece has been issued into
+// the slot (its index is the slot's last issue), then for the slot's mbarrier
+// phase of that piece. The ring's rule: every consumer of a piece waits here
+// before it (or anyone) refills the slot with the piece ns ahead, so a slot
+// holds at most one piece in flight, and once piece i is the slot's last issue
+// the barrier's current phase is piece i's and the parity wait cannot match an
+// older phase. (Two consumer groups take alternate pieces, so with an odd
+// number of slots a group reaches pieces whose slot the other group refills.)
+// False if either wait gave up.
+__device__ __forceinline__ bool ring_wait(const LayerLayout& L, uint8_t* smem, int i) {
+    const int slot = i % L.ns;
+    const volatile int* last = reinterpret_cast<const volatile int*>(smem + L.last);
+    if (last[slot] != i) {
+        const unsigned long long t0 = globaltimer_ns();
+        for (unsigned it = 0; last[slot] != i; ++it)
+            if (globaltimer_ns() - t0 > kSlotTimeoutNs || it > kSlotMaxPolls) return false;
+    }
+    return mbar_wait(smem_u32(smem + L.bars) + slot * 8, (uint32_t)((i / L.ns) & 1));
+}
+
 // Waits (bounded) for the last piece issued into every slot; used before the
 // CTA exits so no copy is in flight into its shared memory.
 __device__ __forceinline__ void drain_ring(const LayerLayout& L, uint8_t* smem, int n_issued_max) {
@@ -697,9 +717,13 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             const int tok = col < np ? pair_token(pair_at(s, d, col), T, k) : T;
             const uint16_t* brow = xg + (size_t)tok * ldx;
             float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+            // every item waits for its piece, a missed unit's too (whose piece
+            // carries no bytes): the group refills the slot after the item, and
+            // a slot may only be refilled once its current piece has been
+            // issued, that is once the piece before it was consumed
+            if (!ring_wait(L, smem, j)) slot_err = 1;
             if (!Dg) {
-                // resident: the tile is (or will be) in slot j % ns
-                if (!mbar_wait(bars + slot * 8, (uint32_t)((j / L.ns) & 1))) slot_err = 1;
+                // resident: the tile is in slot j % ns
                 const uint8_t* pg = ring + (size_t)slot * L.slot;
                 const uint8_t* pu = pg + L.gl;
                 const uint32_t len0 = (uint32_t)KC * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
@@ -794,7 +818,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
             for (int pc = 0; pc < q.dpr; ++pc) {
                 const int i = q.n_gu + r * q.dpr + pc;
                 const int slot = i % L.ns;
-                if (!mbar_wait(bars + slot * 8, (uint32_t)((i / L.ns) & 1))) slot_err = 1;
+                if (!ring_wait(L, smem, i)) slot_err = 1;
                 const int u0 = pc * L.m;
                 const int nup = min(L.m, n_units - u0);
                 const uint8_t* pd = ring + (size_t)slot * L.slot;

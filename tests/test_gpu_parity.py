@@ -207,9 +207,25 @@ def test_one_kernel_and_three_kernel_decode_agree_bitwise(fmt, pool_mode, E, T):
     # / down kernels give the same bits: ids, slots, fills, outputs, final
     # state and counters; both match the oracle.
     k = 4 if E >= 40 else 2
-    w = scaled(WORKLOADS["flash_next_nvfp4"], name="fused", L=3, E=E, k=k, H=512, I=192, fmt=fmt,
+    one_vs_three_kernels(fmt, pool_mode, E, T, k, H=512, I=192, L=3, steps=6, has_shared=fmt in ("nvfp4", "q4_0"))
+
+
+@pytest.mark.parametrize("fmt,H,I,T,k,has_shared", [
+    ("fp8_b128", 2048, 512, 8, 4, False),   # one ring slot
+    ("q4_0", 2048, 512, 4, 8, False),       # three ring slots, refilled
+    ("nvfp4", 2048, 768, 4, 4, True),       # three ring slots, shared expert
+    ("bf16", 1024, 256, 2, 4, False)])      # three ring slots
+def test_one_kernel_decode_with_a_small_ring(fmt, H, I, T, k, has_shared):
+    # Large tiles leave room for one or three weight slots in shared memory,
+    # so the two consumer groups of the one-kernel decode refill slots the
+    # other group reads next; results stay those of the three kernels.
+    one_vs_three_kernels(fmt, "per_layer", 64, T, k, H=H, I=I, L=2, steps=4, has_shared=has_shared)
+
+
+def one_vs_three_kernels(fmt, pool_mode, E, T, k, H, I, L, steps, has_shared):
+    w = scaled(WORKLOADS["flash_next_nvfp4"], name="fused", L=L, E=E, k=k, H=H, I=I, fmt=fmt,
                pool_mode=pool_mode, slots_per_layer=max(T * k + 3, 12), pool_bytes=0.0,
-               has_shared=fmt in ("nvfp4", "q4_0"), bias=True, streams=(T,), steps=6, rho=0.7)
+               has_shared=has_shared, bias=True, streams=(T,), steps=steps, rho=0.7)
     import oracle
     sb = oracle.slot_bytes(fmt, w.H, w.I)
     if pool_mode == "shared":
