@@ -21,6 +21,7 @@ def test_config_defaults():
     pec.load().moe_config_default(ctypes.byref(c))
     assert c.norm_topk == 1 and c.max_cache_tokens == 32 and c.prefill_group == 32 and c.max_tokens == 32
     assert c.upload_mode == 0 and c.pool_mode == 0
+    assert c.split_decode == 0  # decode calls that fit run as one persistent kernel
 
 
 @pytest.mark.parametrize("kw,status", [
