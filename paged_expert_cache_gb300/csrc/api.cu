@@ -128,6 +128,7 @@ moe_status_t init_tables(moe_cache_t* h) {
     CK(h, cudaMemset(d.stats, 0, 16 * sizeof(unsigned long long)));
     if (h->scr.grid_bar) CK(h, cudaMemset(h->scr.grid_bar, 0, sizeof(unsigned)));
     if (h->scr.err) CK(h, cudaMemset(h->scr.err, 0, sizeof(unsigned)));
+    if (h->scr.logit_ctr) CK(h, cudaMemset(h->scr.logit_ctr, 0, 2 * sizeof(unsigned)));
     if (d.trace_count) CK(h, cudaMemset(d.trace_count, 0, sizeof(unsigned long long)));
     memset(h->memcpy_upload_ns, 0, sizeof(h->memcpy_upload_ns));
     return MOE_OK;
@@ -293,6 +294,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.tiles_done, 1);
     DA(s.grid_bar, 1);
     DA(s.err, 1);
+    DA(s.logit_ctr, 2);
     if (h->maxT > c.max_cache_tokens) {
         DA(s.gemm_items, moe::gemm_max_items(P, U));
         DA(s.gemm_count, 1);
@@ -308,7 +310,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         cudaMemset(s.copy_done, 0, 4) != cudaSuccess || cudaMemset(s.copy_t0, 0xff, 8) != cudaSuccess ||
         cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess ||
         cudaMemset(s.tiles_done, 0, 4) != cudaSuccess || cudaMemset(s.grid_bar, 0, 4) != cudaSuccess ||
-        cudaMemset(s.err, 0, 4) != cudaSuccess)
+        cudaMemset(s.err, 0, 4) != cudaSuccess || cudaMemset(s.logit_ctr, 0, 8) != cudaSuccess)
         return bail(MOE_ERR_CUDA, "scratch initialisation failed");
     if (c.upload_mode == MOE_UPLOAD_MEMCPY) {
         e = cudaHostAlloc((void**)&h->host_fill, sizeof(int) * (2 + 2 * U), cudaHostAllocDefault);

@@ -97,6 +97,7 @@ struct Scratch {
     unsigned* grid_bar;     // arrival counter of the fused layer kernel's grid barriers
     unsigned* err;          // sticky device error bits (1: a grid barrier timed out, 2: a weight-slot
                             // wait timed out, 4: a prefill GEMM wait timed out)
+    unsigned* logit_ctr;    // [2] logit CTAs done, per call parity (one-kernel decode)
     int2* gemm_items;       // prefill GEMM work list: (unit, 128-pair tile)
     int* gemm_count;        // its length
 };

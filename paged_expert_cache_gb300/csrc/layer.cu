@@ -523,7 +523,15 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     const int U = min(n_ids, E) + 1;
     const int P = n_ids + (c.has_shared ? T : 0);
     const int pool = c.pool_mode ? 0 : a.layer;
-    const int rows = (E + G - 1) / G;
+    // logits: warp w of CTA b < NL computes expert 16 b + w, so only the first
+    // NL CTAs, which start first on the SMs the previous call frees, gate
+    // the ranking
+    const int rows = E < kLWarps ? E : kLWarps;
+    const int NL = (E + kLWarps - 1) / kLWarps;
+    // When the committing CTA owns no output row tile it commits after the
+    // second barrier; then nothing is written that any CTA reads before it,
+    // and the first barrier reduces to waiting for the logit CTAs.
+    const bool logit_wait = G - 1 >= H / 16;
     const LayerLayout L = layer_layout(FMT, E, c.K, k, H, I, T, c.has_shared, rows);
     UnitDesc* sd = reinterpret_cast<UnitDesc*>(smem + L.sd);
     int* sids = reinterpret_cast<int*>(smem + L.ids);
@@ -539,10 +547,10 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     }
 
     // ---- 1. logits ---------------------------------------------------------
-    // warp j of CTA b owns expert b + j G; its router row does not depend on
+    // warp w of CTA b owns expert 16 b + w; its router row does not depend on
     // the preceding grid, so its copy to shared memory starts before the wait
     // (each lane copies, and later reads, its own 16-byte vectors)
-    const int e_mine = b + G * warp;
+    const int e_mine = b * kLWarps + warp;
     uint16_t* wr = reinterpret_cast<uint16_t*>(smem + L.wr) + (size_t)warp * H;
     if (e_mine < E)
         for (int i = 0; i < H / 256; ++i)
@@ -606,7 +614,33 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     }
     if (e_mine < E)
         for (int t = 0; t < T; ++t) router_logit_row(c, a, xs + (size_t)t * H, wr, t, e_mine, s.logits, s.bounds);
-    if (!grid_barrier(s.grid_bar, s.err, phase)) return;  // nothing is in flight yet
+    const unsigned parity = phase ? 1u : 0u;  // thread 0: this call's parity (one grid barrier per call)
+    if (logit_wait) {
+        // the logit CTAs announce their logits; every CTA waits for all NL
+        __shared__ int lw_ok;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned* ctr = s.logit_ctr + parity;
+            if (b < NL) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(ctr) : "memory");
+            const unsigned long long t0 = globaltimer_ns();
+            int good = 1;
+            for (unsigned it = 0;; ++it) {
+                unsigned cur;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(cur) : "l"(ctr) : "memory");
+                if (cur >= (unsigned)NL) break;
+                if (globaltimer_ns() - t0 > kBarrierTimeoutNs || it > kBarrierMaxPolls) {
+                    atomicOr(s.err, 1u);
+                    good = 0;
+                    break;
+                }
+            }
+            lw_ok = good;
+        }
+        __syncthreads();
+        if (!lw_ok) return;  // nothing is in flight yet
+    } else if (!grid_barrier(s.grid_bar, s.err, phase)) {
+        return;  // nothing is in flight yet
+    }
 
     // ---- 2. top-k and plan in every CTA ----------------------------------
     if (T == 1 && E <= 256) {
@@ -628,7 +662,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     // on a fresh copy of the pool's state after (nothing else writes that state
     // during the call, and every CTA read it before the first barrier).
     const bool commit = b == G - 1;
-    const bool defer = commit && b >= H / 16;
+    const bool defer = commit && logit_wait;
     if (commit) {
         for (int i = tid; i < n_ids; i += kLThreads) {
             s.ids[i] = sids[i];
@@ -783,6 +817,9 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     }
 
     // ---- 4. down projection + combine by row tiles -------------------------
+    // every CTA is past its logit wait: clear this parity's counter for the
+    // call two ahead (the next call uses the other one)
+    if (logit_wait && b == 0 && tid == 0) s.logit_ctr[parity] = 0u;
     if (defer) {
         // this CTA has no row tile: its ring and staging are free for the plan
         stage_state();
@@ -911,8 +948,8 @@ size_t layer_smem_bytes(const CacheDev& c, int T) {
     const int P = T * c.k + (c.has_shared ? T : 0);
     const int G = layer_ctas();
     // every expert needs a warp of some CTA
-    if (P > kLayerMaxPairs || G <= 0 || (c.E + G - 1) / G > kLWarps) return 0;
-    const LayerLayout L = layer_layout(c.fmt, c.E, c.K, c.k, c.H, c.I, T, c.has_shared, (c.E + G - 1) / G);
+    if (P > kLayerMaxPairs || G <= 0 || (c.E + kLWarps - 1) / kLWarps > G) return 0;
+    const LayerLayout L = layer_layout(c.fmt, c.E, c.K, c.k, c.H, c.I, T, c.has_shared, c.E < kLWarps ? c.E : kLWarps);
     return L.ns >= 1 && L.total <= kLayerSmemLimit ? L.total : 0;
 }
 
