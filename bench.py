@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU sample")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
-    ap.add_argument("--split", action="store_true", help="route, gate/up and down as three kernels per decode call")
+    ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
+                    help="decode launch mode (auto: one kernel for single-token calls on per-layer pools)")
     ap.add_argument("--prefill", action="store_true",
                     help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()
@@ -273,7 +274,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
-                          max_tokens=max(T, 1), device=local, split_decode=args.split)
+                          max_tokens=max(T, 1), device=local, decode=args.decode)
     t_setup = time.perf_counter()
     cache = pec.MoECache(cfg)
     buf = None

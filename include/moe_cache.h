@@ -88,6 +88,19 @@ typedef enum { MOE_POOL_PER_LAYER = 0, MOE_POOL_SHARED = 1 } moe_pool_mode_t;
  *                      "Inside llama.cpp PR #29887"]. */
 typedef enum { MOE_UPLOAD_PULL = 0, MOE_UPLOAD_MEMCPY = 1 } moe_upload_mode_t;
 
+/* How a decode call (T <= max_cache_tokens) is launched. The one-kernel path
+ * runs the whole call as one persistent kernel (one CTA per SM, two bounded
+ * grid-wide waits, the weight tiles streamed into shared memory by bulk
+ * copies); it takes calls with T <= 8, T*k (+T shared) <= 48 and PULL
+ * uploads whose shared-memory layout fits. The three-kernel path runs route,
+ * gate/up and down kernels. */
+typedef enum {
+    MOE_DECODE_AUTO = 0,          /* one kernel for single-token calls on per-layer pools (where it
+                                     measured faster), three kernels otherwise */
+    MOE_DECODE_THREE_KERNELS = 1, /* always three kernels */
+    MOE_DECODE_ONE_KERNEL = 2     /* one kernel for every call that fits */
+} moe_decode_mode_t;
+
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_experts;      /* E routed experts per layer, 1..1024 */
@@ -105,16 +118,12 @@ typedef struct {
     int32_t prefill_group;    /* experts staged per prefill group (32) */
     int32_t max_tokens;       /* largest T of any call (sizes scratch) */
     int32_t device;           /* CUDA device ordinal */
-    int32_t split_decode;     /* 0 (default): a decode call that fits (T <= 8, T*k (+T shared) <= 48,
-                                 PULL uploads) runs as one persistent kernel, one CTA per SM with
-                                 two bounded grid barriers, its weight tiles streamed into shared
-                                 memory by bulk copies; other calls take the three kernels.
-                                 1: always three kernels (route, gate/up, down). Both give bitwise
-                                 identical results. */
+    int32_t split_decode;     /* moe_decode_mode_t: how decode calls are launched (default
+                                 MOE_DECODE_AUTO). Every mode gives bitwise identical results. */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
- * max_tokens 32, upload PULL, per-layer pools, split_decode 0; shape fields
+ * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO; shape fields
  * zero. */
 void moe_config_default(moe_config_t* cfg);
 
@@ -143,7 +152,7 @@ typedef struct {
     uint64_t pool_device_bytes;   /* slot pool(s) in HBM */
     uint64_t store_host_bytes;    /* pinned host store, every expert of every layer */
     uint64_t scratch_device_bytes;
-    uint64_t fused_decode_calls;  /* decode calls launched as one kernel (split_decode 0) */
+    uint64_t fused_decode_calls;  /* decode calls launched as one kernel */
     uint64_t split_decode_calls;  /* decode calls launched as route, gate/up, down kernels */
 } moe_info_t;
 
@@ -243,7 +252,7 @@ moe_status_t moe_cache_read_slot(moe_cache_t* h, int32_t pool, int32_t slot, voi
  * forward launches is bracketed by CUDA events on the forward's stream (do
  * not enable it while capturing a CUDA graph). Stages: 0 router + top-k +
  * plan, 1 miss copies, 2 gate/up + SwiGLU, 3 down + combine, 4 prefill top-k,
- * 5 prefill plan, 6 the whole decode call in one kernel (split_decode 0). */
+ * 5 prefill plan, 6 the whole decode call in one kernel. */
 #define MOE_NUM_STAGES 7
 typedef struct {
     double ms[MOE_NUM_STAGES];         /* summed event time per stage */

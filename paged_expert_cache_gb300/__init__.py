@@ -20,6 +20,7 @@ OK, ERR_INVALID, ERR_CAPACITY, ERR_CUDA, ERR_OOM, ERR_STATE, ERR_TIMEOUT = range
 FORMATS = {"bf16": 0, "q4_0": 1, "fp8_b128": 2, "nvfp4": 3}
 POOL_MODES = {"per_layer": 0, "shared": 1}
 UPLOAD_MODES = {"pull": 0, "memcpy": 1}
+DECODE_MODES = {"auto": 0, "three_kernels": 1, "one_kernel": 2}
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_OOM",
                 5: "MOE_ERR_STATE", 6: "MOE_ERR_TIMEOUT"}
 
@@ -121,7 +122,7 @@ def _check(st, handle=None):
 
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
-                max_tokens=32, device=0, split_decode=False):
+                max_tokens=32, device=0, decode="auto"):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -136,7 +137,7 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.prefill_group = prefill_group
     c.max_tokens = max_tokens
     c.device = device
-    c.split_decode = 1 if split_decode else 0
+    c.split_decode = DECODE_MODES[decode] if isinstance(decode, str) else int(decode)
     return c
 
 

@@ -21,7 +21,7 @@ def test_config_defaults():
     pec.load().moe_config_default(ctypes.byref(c))
     assert c.norm_topk == 1 and c.max_cache_tokens == 32 and c.prefill_group == 32 and c.max_tokens == 32
     assert c.upload_mode == 0 and c.pool_mode == 0
-    assert c.split_decode == 0  # decode calls that fit run as one persistent kernel
+    assert c.split_decode == 0  # automatic choice of the decode launch
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -34,6 +34,7 @@ def test_config_defaults():
     (dict(L=1, E=16, k=4, H=256, I=128, slots_per_layer=3), pec.ERR_CAPACITY),
     (dict(L=1, E=16, k=2, H=256, I=128, pool_mode="shared", pool_bytes=196608 * 2 - 1), pec.ERR_CAPACITY),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, max_cache_tokens=33), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, decode=3), pec.ERR_INVALID),
 ])
 def test_invalid_configurations_are_refused(kw, status):
     args = dict(kw)

@@ -203,7 +203,7 @@ def test_exact_ties_rank_the_lower_expert_first():
     ("q4_0", "per_layer", 64, 1), ("q4_0", "shared", 64, 3), ("fp8_b128", "per_layer", 40, 8),
     ("nvfp4", "shared", 160, 2), ("bf16", "per_layer", 16, 4), ("nvfp4", "per_layer", 160, 4)])
 def test_one_kernel_and_three_kernel_decode_agree_bitwise(fmt, pool_mode, E, T):
-    # The persistent one-kernel decode (split_decode 0) and the route / gate/up
+    # The persistent one-kernel decode and the route / gate/up
     # / down kernels give the same bits: ids, slots, fills, outputs, final
     # state and counters; both match the oracle.
     k = 4 if E >= 40 else 2
@@ -232,7 +232,7 @@ def one_vs_three_kernels(fmt, pool_mode, E, T, k, H, I, L, steps, has_shared):
         w = scaled(w, pool_bytes=sb * (T * k + 6) + 5)
     runs = {}
     for split in (False, True):
-        st = Setup(w, split_decode=split)
+        st = Setup(w, decode="three_kernels" if split else "one_kernel")
         orc = OracleRun(w, st.info["slot_bytes"])
         xs = {l: st.hiddens(l, T, w.steps) for l in range(w.L)}
         ys, recs = [], []
