@@ -345,7 +345,7 @@ __device__ __forceinline__ Pieces make_pieces(int b, int G, int RT, int RTD, int
 // arrival on the slot's mbarrier (missed units' bytes are not copied: their
 // consumers read the host store or the slot directly). One thread.
 template <int FMT>
-__device__ __noinline__ void issue_piece(int i, const Pieces& q, const LayerLayout& L, const UnitDesc* sd, uint8_t* smem, int H,
+__device__ __forceinline__ void issue_piece(int i, const Pieces& q, const LayerLayout& L, const UnitDesc* sd, uint8_t* smem, int H,
                             int I, uint64_t pol) {
     const int slot = i % L.ns;
     const uint32_t bar = smem_u32(smem + L.bars) + slot * 8;
@@ -433,6 +433,11 @@ __device__ __forceinline__ void drain_ring(const LayerLayout& L, uint8_t* smem, 
 }
 
 
+// The gate and up accumulators of one warp's share of a gate/up item.
+struct GateUpAcc {
+    float g[4], u[4];
+};
+
 // One gate/up item (16-row tile rt) of a missed unit, read from the mapped
 // host store over the host link (Wg: gate; up follows at the matrix stride)
 // and written through to its slot (Dg) as it is read, by one group of eight
@@ -443,8 +448,13 @@ __device__ __forceinline__ void drain_ring(const LayerLayout& L, uint8_t* smem, 
 // is paid about once per item. Out of line: calls with misses are bound by
 // the host link, and the all-hit path keeps a short instruction stream.
 template <int FMT>
-__device__ __noinline__ void pull_item(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
-                                       int lane, const uint16_t* brow, float (&ag)[4], float (&au)[4]) {
+__device__ __noinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
+                                            int lane, const uint16_t* brow) {
+    GateUpAcc r;
+    float (&ag)[4] = r.g;
+    float (&au)[4] = r.u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ag[i] = au[i] = 0.f;
     constexpr bool kNib = FMT == FMT_Q4_0 || FMT == FMT_NVFP4;
     constexpr int CIF = kNib ? 4 : (FMT == FMT_FP8_B128 ? 2 : 1);  // chunks in flight per matrix
     constexpr int DS = kNib ? 2 : (FMT == FMT_FP8_B128 ? 2 : 1);    // down-share vectors in flight
@@ -508,10 +518,12 @@ __device__ __noinline__ void pull_item(const uint8_t* Wg, uint8_t* Dg, int I, in
             if (vi < v1) stg_stream(dst + vi * 16, buf[i]);
         }
     }
+    return r;
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, RouteArgs a, float* __restrict__ out) {
+__global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
+                                                      const __grid_constant__ RouteArgs a, float* __restrict__ out) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ unsigned long long clk;
     __shared__ int rerank;
@@ -532,7 +544,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
     // second barrier; then nothing is written that any CTA reads before it,
     // and the first barrier reduces to waiting for the logit CTAs.
     const bool logit_wait = G - 1 >= H / 16;
-    const LayerLayout L = layer_layout(FMT, E, c.K, k, H, I, T, c.has_shared, rows);
+    // the layout lives in shared memory: its fields are read once per phase,
+    // and held in registers they would be spilled
+    __shared__ LayerLayout sL;
+    if (threadIdx.x == 0) sL = layer_layout(FMT, E, c.K, k, H, I, T, c.has_shared, rows);
+    __syncthreads();
+    const LayerLayout& L = sL;
     UnitDesc* sd = reinterpret_cast<UnitDesc*>(smem + L.sd);
     int* sids = reinterpret_cast<int*>(smem + L.ids);
     float* swts = reinterpret_cast<float*>(smem + L.wts);
@@ -594,6 +611,17 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         }
         cp_async_wait();
         __syncthreads();
+    }
+    // the logits first, announced as soon as they are written: they gate
+    // every CTA's ranking, the f16 copy below only this CTA's expert phase
+    if (e_mine < E)
+        for (int t = 0; t < T; ++t) router_logit_row(c, a, xs + (size_t)t * H, wr, t, e_mine, s.logits, s.bounds);
+    const unsigned parity = phase ? 1u : 0u;  // thread 0: this call's parity (one grid barrier per call)
+    if (logit_wait && b < NL) {
+        __syncthreads();
+        if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(s.logit_ctr + parity) : "memory");
+    }
+    {
         // f16 copy of the tokens for the expert B operand (converted as the
         // gate/up kernel does); row T is zero
         for (int i = tid; i < T * (H / 8); i += kLThreads) {
@@ -612,16 +640,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         }
         for (int i = tid; i < ldx / 2; i += kLThreads) reinterpret_cast<uint32_t*>(xg + (size_t)T * ldx)[i] = 0u;
     }
-    if (e_mine < E)
-        for (int t = 0; t < T; ++t) router_logit_row(c, a, xs + (size_t)t * H, wr, t, e_mine, s.logits, s.bounds);
-    const unsigned parity = phase ? 1u : 0u;  // thread 0: this call's parity (one grid barrier per call)
     if (logit_wait) {
-        // the logit CTAs announce their logits; every CTA waits for all NL
+        // every CTA waits until all NL logit CTAs have announced theirs
         __shared__ int lw_ok;
         __syncthreads();
         if (tid == 0) {
-            unsigned* ctr = s.logit_ctr + parity;
-            if (b < NL) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(ctr) : "memory");
+            const unsigned* ctr = s.logit_ctr + parity;
             const unsigned long long t0 = globaltimer_ns();
             int good = 1;
             for (unsigned it = 0;; ++it) {
@@ -777,7 +801,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
                 // missed: read the tile from the mapped host store over the
                 // host link and write it through to the slot
                 if (gtid == 0) atomicMin(s.copy_t0, globaltimer_ns());
-                pull_item<FMT>(Wg, Dg, I, H, rt, gtid, gw, lane, brow, ag, au);
+                const GateUpAcc r = pull_item<FMT>(Wg, Dg, I, H, rt, gtid, gw, lane, brow);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ag[i] = r.g[i];
+                    au[i] = r.u[i];
+                }
             }
             const int g = lane >> 2, qd = lane & 3;
             float* rg = red + (size_t)(gw * 2) * 128;
@@ -852,55 +881,73 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(CacheDev c, Scratch s, R
         for (int r = 0; r < q.n_rt; ++r) {
             const int rt = b + G * r;
             const uint32_t soff = scale_soff<FMT>(H, I, rt);
-            for (int pc = 0; pc < q.dpr; ++pc) {
-                const int i = q.n_gu + r * q.dpr + pc;
-                const int slot = i % L.ns;
-                if (!ring_wait(L, smem, i)) slot_err = 1;
-                const int u0 = pc * L.m;
-                const int nup = min(L.m, n_units - u0);
-                const uint8_t* pd = ring + (size_t)slot * L.slot;
-                for (int itm = warp; itm < nup * ncg; itm += kLWarps) {
-                    const int v = itm / ncg, cgi = itm - v * ncg;
-                    const UnitDesc& d = sd[u0 + v];
-                    const int col = lane & 7;
-                    const int pr = col < d.np ? d.pair8[col] : P;
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // one (unit, chunk group) item: the unit's partial sums of this row
+            // tile over its chunk group (pdv: the unit's down rows in the ring)
+            auto down_item = [&](int u, int cgi, const uint8_t* pdv) {
+                const UnitDesc& d = sd[u];
+                const int col = lane & 7;
+                const int pr = col < d.np ? d.pair8[col] : P;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int ci = 0; ci < kDRChunks; ++ci) {
-                        const int kc = cgi * kDRChunks + ci;
-                        if (kc >= KCD) break;
-                        Chunk<FMT> ch;
-                        if (d.dst) {
-                            // a missed record: written to its slot by the gate/up pass
-                            load_chunk_cg<FMT>(reinterpret_cast<const uint8_t*>(d.dst) + 2 * mgu, H, I, rt, kc, lane, ch);
-                        } else {
-                            smem_chunk<FMT>(pd + (size_t)v * L.du, len0, soff, kc, lane, ch);
-                        }
-                        uint32_t bf[2][4][2];
-                        const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
-                        const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
-                        ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
-                        ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
-                        ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
-                        ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
-                        mma_chunk<FMT, 2>(ch, bf, acc);
+                for (int ci = 0; ci < kDRChunks; ++ci) {
+                    const int kc = cgi * kDRChunks + ci;
+                    if (kc >= KCD) break;
+                    Chunk<FMT> ch;
+                    if (d.dst) {
+                        // a missed record: written to its slot by the gate/up pass
+                        load_chunk_cg<FMT>(reinterpret_cast<const uint8_t*>(d.dst) + 2 * mgu, H, I, rt, kc, lane, ch);
+                    } else {
+                        smem_chunk<FMT>(pdv, len0, soff, kc, lane, ch);
                     }
-                    const float gd = d.g[2];
+                    uint32_t bf[2][4][2];
+                    const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                    const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+                    ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
+                    ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
+                    ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
+                    ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
+                    mma_chunk<FMT, 2>(ch, bf, acc);
+                }
+                const float gd = d.g[2];
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
+                for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-                        for (int c2 = 0; c2 < 2; ++c2) {
-                            const int cc = 2 * qd + c2;
-                            if (cc < d.np) {
-                                const int pair = d.pair8[cc];
-                                ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
-                            }
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int cc = 2 * qd + c2;
+                        if (cc < d.np) {
+                            const int pair = d.pair8[cc];
+                            ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
                         }
                     }
                 }
+            };
+            if (q.n <= L.ns) {
+                // every piece was requested at the start and no slot is
+                // refilled: all units' items in one pass, each waiting for
+                // its own piece
+                for (int itm = warp; itm < n_units * ncg; itm += kLWarps) {
+                    const int u = itm / ncg, cgi = itm - u * ncg, pc = u / L.m;
+                    const int i = q.n_gu + r * q.dpr + pc;
+                    if (!ring_wait(L, smem, i)) slot_err = 1;
+                    down_item(u, cgi, ring + (size_t)(i % L.ns) * L.slot + (size_t)(u - pc * L.m) * L.du);
+                }
                 __syncthreads();
-                // the slot is consumed: refill it with the piece ns ahead
-                if (tid == 0 && i + L.ns < q.n) issue_piece<FMT>(i + L.ns, q, L, sd, smem, H, I, pol);
+            } else {
+                for (int pc = 0; pc < q.dpr; ++pc) {
+                    const int i = q.n_gu + r * q.dpr + pc;
+                    const int slot = i % L.ns;
+                    if (!ring_wait(L, smem, i)) slot_err = 1;
+                    const int u0 = pc * L.m;
+                    const int nup = min(L.m, n_units - u0);
+                    const uint8_t* pd = ring + (size_t)slot * L.slot;
+                    for (int itm = warp; itm < nup * ncg; itm += kLWarps) {
+                        const int v = itm / ncg, cgi = itm - v * ncg;
+                        down_item(u0 + v, cgi, pd + (size_t)v * L.du);
+                    }
+                    __syncthreads();
+                    // the slot is consumed: refill it with the piece ns ahead
+                    if (tid == 0 && i + L.ns < q.n) issue_piece<FMT>(i + L.ns, q, L, sd, smem, H, I, pol);
+                }
             }
             for (int i = tid; i < T * 16; i += kLThreads) {
                 const int t = i >> 4, row = i & 15;
