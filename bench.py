@@ -493,6 +493,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2: each step reads ~1 GB of distinct expert bytes from an "
                          f"{info['pool_device_bytes'] / 1e9:.1f} GB slot pool"},
         "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
+        "topk_fp64_reranks": s1["topk_fp64_rerank"] - s0["topk_fp64_rerank"],
         "upload_gbs": up_bytes / up_ns if up_ns else None, "host_link_h2d_gbs": link_gbs,
         "expert_ffn_all_hit": {"gbs": ffn_gbs_hit, "frac_of_measured": ffn_gbs_hit / peaks["hbm_gbs"] if ffn_gbs_hit
                                else None, "frac_of_8tbs": ffn_gbs_hit / 8000.0 if ffn_gbs_hit else None,

@@ -50,6 +50,9 @@ namespace moe {
 
 constexpr int kLThreads = 512;
 constexpr int kLWarps = kLThreads / 32;
+// Warps of a CTA that compute router logits, one expert each: one per
+// scheduler, so each logit's instruction stream issues without competing.
+constexpr int kLogitWarps = 4;
 constexpr int kLayerMaxTokens = 8;    // tokens per call (a unit has at most 8 pairs: one n-tile)
 constexpr int kLayerMaxPairs = 48;    // T * k (+ T for the shared expert)
 constexpr int kLayerRankWarps = 4;    // warps that rank tokens (each needs a TopkSmem)
@@ -443,20 +446,21 @@ struct GateUpAcc {
 // and written through to its slot (Dg) as it is read, by one group of eight
 // warps (gw: the warp in the group, gtid: the thread); plus the item's share
 // of the record's down matrix, copied to the slot, so the whole record crosses
-// the link in this pass. All of a thread's loads for the gate/up chunks and
-// the first batch of its down share are in flight at once: the link's latency
-// is paid about once per item. Out of line: calls with misses are bound by
-// the host link, and the all-hit path keeps a short instruction stream.
+// the link in this pass. Two chunk loads per matrix (4-bit formats; one
+// otherwise) and the first batch of the down share are in flight at once.
+// Inlined: a call would make the caller save its live registers around it,
+// and those saves, in local memory that misses the small L1 left beside the
+// shared memory, cost the all-hit path more than the deeper pull gains.
 template <int FMT>
-__device__ __noinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid, int gw,
-                                            int lane, const uint16_t* brow) {
+__device__ __forceinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, int I, int H, int rt, int gtid,
+                                               int gw, int lane, const uint16_t* brow) {
     GateUpAcc r;
     float (&ag)[4] = r.g;
     float (&au)[4] = r.u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) ag[i] = au[i] = 0.f;
     constexpr bool kNib = FMT == FMT_Q4_0 || FMT == FMT_NVFP4;
-    constexpr int CIF = kNib ? 4 : (FMT == FMT_FP8_B128 ? 2 : 1);  // chunks in flight per matrix
+    constexpr int CIF = kNib ? 2 : 1;  // chunks in flight per matrix
     constexpr int DS = kNib ? 2 : (FMT == FMT_FP8_B128 ? 2 : 1);    // down-share vectors in flight
     const uint64_t mgu = matrix_stride(FMT, I, H);
     const uint8_t* Wu = Wg + mgu;
@@ -521,7 +525,9 @@ __device__ __noinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, int 
     return r;
 }
 
-template <int FMT>
+// kOneToken: the instantiation for one token and at most 256 experts, with
+// the many-token ranking left out (its registers would crowd the rest).
+template <int FMT, bool kOneToken>
 __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
                                                       const __grid_constant__ RouteArgs a, float* __restrict__ out) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -530,16 +536,16 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     __shared__ int slot_err;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
-    const int E = c.E, H = c.H, I = c.I, k = c.k, T = a.T;
+    const int E = c.E, H = c.H, I = c.I, k = c.k, T = kOneToken ? 1 : a.T;
     const int n_ids = T * k;
     const int U = min(n_ids, E) + 1;
     const int P = n_ids + (c.has_shared ? T : 0);
     const int pool = c.pool_mode ? 0 : a.layer;
-    // logits: warp w of CTA b < NL computes expert 16 b + w, so only the first
-    // NL CTAs, which start first on the SMs the previous call frees, gate
-    // the ranking
-    const int rows = E < kLWarps ? E : kLWarps;
-    const int NL = (E + kLWarps - 1) / kLWarps;
+    // logits: warp w < 4 of CTA b < NL computes expert 4 b + w, so only the
+    // first NL CTAs, which start first on the SMs the previous call frees,
+    // gate the ranking
+    const int rows = E < kLogitWarps ? E : kLogitWarps;
+    const int NL = (E + kLogitWarps - 1) / kLogitWarps;
     // When the committing CTA owns no output row tile it commits after the
     // second barrier; then nothing is written that any CTA reads before it,
     // and the first barrier reduces to waiting for the logit CTAs.
@@ -564,10 +570,10 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     }
 
     // ---- 1. logits ---------------------------------------------------------
-    // warp w of CTA b owns expert 16 b + w; its router row does not depend on
-    // the preceding grid, so its copy to shared memory starts before the wait
-    // (each lane copies, and later reads, its own 16-byte vectors)
-    const int e_mine = b * kLWarps + warp;
+    // warp w < 4 of CTA b owns expert 4 b + w; its router row does not depend
+    // on the preceding grid, so its copy to shared memory starts before the
+    // wait (each lane copies, and later reads, its own 16-byte vectors)
+    const int e_mine = warp < kLogitWarps ? b * kLogitWarps + warp : E;
     uint16_t* wr = reinterpret_cast<uint16_t*>(smem + L.wr) + (size_t)warp * H;
     if (e_mine < E)
         for (int i = 0; i < H / 256; ++i)
@@ -667,7 +673,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     }
 
     // ---- 2. top-k and plan in every CTA ----------------------------------
-    if (T == 1 && E <= 256) {
+    if (kOneToken) {
         // one token: every expert ranked at once by its own thread
         const TopkSmem tw = topk_layout(smem + L.topk, E);
         topk_rank_block(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
@@ -995,26 +1001,37 @@ size_t layer_smem_bytes(const CacheDev& c, int T) {
     const int P = T * c.k + (c.has_shared ? T : 0);
     const int G = layer_ctas();
     // every expert needs a warp of some CTA
-    if (P > kLayerMaxPairs || G <= 0 || (c.E + kLWarps - 1) / kLWarps > G) return 0;
-    const LayerLayout L = layer_layout(c.fmt, c.E, c.K, c.k, c.H, c.I, T, c.has_shared, c.E < kLWarps ? c.E : kLWarps);
+    if (P > kLayerMaxPairs || G <= 0 || (c.E + kLogitWarps - 1) / kLogitWarps > G) return 0;
+    const LayerLayout L =
+        layer_layout(c.fmt, c.E, c.K, c.k, c.H, c.I, T, c.has_shared, c.E < kLogitWarps ? c.E : kLogitWarps);
     return L.ns >= 1 && L.total <= kLayerSmemLimit ? L.total : 0;
 }
 
-template <int FMT>
-static bool layer_launch(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, size_t sm,
-                         cudaStream_t st, bool pdl) {
+template <int FMT, bool kOneToken>
+static bool layer_launch_as(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, size_t sm,
+                            cudaStream_t st, bool pdl) {
     static size_t set = 0;
     if (sm > set) {
-        if (cudaFuncSetAttribute(k_layer<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+        if (cudaFuncSetAttribute(k_layer<FMT, kOneToken>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+            cudaSuccess)
             return false;
         set = sm;
     }
     // one CTA per SM, all resident: the grid barriers rely on it
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer<FMT>, kLThreads, sm) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer<FMT, kOneToken>, kLThreads, sm) !=
+            cudaSuccess ||
         per_sm < 1)
         return false;
-    return launch_ex(k_layer<FMT>, dim3(layer_ctas()), dim3(kLThreads), sm, st, pdl, c, s, a, out) == cudaSuccess;
+    return launch_ex(k_layer<FMT, kOneToken>, dim3(layer_ctas()), dim3(kLThreads), sm, st, pdl, c, s, a, out) ==
+           cudaSuccess;
+}
+
+template <int FMT>
+static bool layer_launch(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, size_t sm,
+                         cudaStream_t st, bool pdl) {
+    if (a.T == 1 && c.E <= 256) return layer_launch_as<FMT, true>(c, s, a, out, sm, st, pdl);
+    return layer_launch_as<FMT, false>(c, s, a, out, sm, st, pdl);
 }
 
 bool launch_layer(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, int bucket, cudaStream_t st,

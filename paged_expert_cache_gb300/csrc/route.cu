@@ -14,7 +14,8 @@ namespace moe {
 // Fused decode routing: all CTAs compute logits; the last CTA to finish
 // prefetches the pool's state, ranks every token and runs the plan.
 template <int NT>
-__global__ void __launch_bounds__(kRouteThreads, 1) k_route(CacheDev c, Scratch s, RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
+                                                         const __grid_constant__ RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     griddep_wait();
     griddep_launch();
@@ -60,7 +61,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(CacheDev c, Scratch 
 }
 
 // Prefill: one warp per token.
-__global__ void __launch_bounds__(kRouteThreads) k_topk(CacheDev c, Scratch s, RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads) k_topk(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
+                                                       const __grid_constant__ RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     griddep_wait();
     const int warp = threadIdx.x >> 5, E = c.E;
@@ -276,7 +278,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 // All CTAs compute logits; the last one to finish ranks every token.
 template <int NT>
-__global__ void __launch_bounds__(kRouteThreads, 1) k_route_noalloc(CacheDev c, Scratch s, RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route_noalloc(const __grid_constant__ CacheDev c,
+                                                                 const __grid_constant__ Scratch s,
+                                                                 const __grid_constant__ RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     router_logits_tile<NT>(c, a, smem, s.logits, s.bounds);
     __threadfence();

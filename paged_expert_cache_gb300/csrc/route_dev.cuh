@@ -315,9 +315,13 @@ __device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
 }
 
 // Top-k of token t by one warp; writes ids and weights of the token.
-static __device__ __noinline__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t, const TopkSmem& w,
-                           int* rerank_flag, int* ids_out, float* wts_out) {
+// The scratch comes as its base address (topk_layout's), not as a TopkSmem:
+// a reference would put the caller's TopkSmem in local memory, and every
+// read of its pointers on the fast path would go there.
+static __device__ __noinline__ void topk_token(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
+                                               uint8_t* wbase, int* rerank_flag, int* ids_out, float* wts_out) {
     const int E = c.E, k = c.k, lane = threadIdx.x & 31;
+    const TopkSmem w = topk_layout(wbase, E);
     stage_cg<float2>(w.z, s.logits + (size_t)t * E, E, lane, 32);
     stage_cg<float>(w.b, s.bounds + (size_t)t * E, E, lane, 32);
     __syncwarp();
@@ -481,7 +485,7 @@ static __device__ void topk_certify_finish(const CacheDev& c, const Scratch& s, 
     if (pair_gt(mx, later)) later = mx;
     const bool ok = __all_sync(0xffffffffu, lane >= k || pair_gt(lower, later));
     if (!ok) {
-        topk_token(c, s, a, t, w, rerank_flag, ids_out, wts_out);
+        topk_token(c, s, a, t, reinterpret_cast<uint8_t*>(w.z64), rerank_flag, ids_out, wts_out);
         return;
     }
     float zref = -INFINITY, sum = 0.f;
@@ -652,7 +656,7 @@ __device__ __forceinline__ void topk_dispatch(const CacheDev& c, const Scratch& 
     else if (c.E <= 128) topk_token_fast<4>(c, s, a, t, w, rerank_flag, ids_out, wts_out);
     else if (c.E <= 256) topk_token_fast<8>(c, s, a, t, w, rerank_flag, ids_out, wts_out);
     else if (c.E <= 512) topk_token_fast<16>(c, s, a, t, w, rerank_flag, ids_out, wts_out);
-    else topk_token(c, s, a, t, w, rerank_flag, ids_out, wts_out);
+    else topk_token(c, s, a, t, reinterpret_cast<uint8_t*>(w.z64), rerank_flag, ids_out, wts_out);
 }
 
 // ---------------------------------------------------------------------------
