@@ -114,7 +114,7 @@ __host__ __device__ inline LayerLayout layer_layout(int fmt, int E, int K, int k
     L.wr = p; p = align16(p + (size_t)rows * H * 2);
     L.plan = p; p = align16(p + plan_layout(nullptr, E, K, n_ids, U, P).bytes);
     L.topk = p; p = align16(p + (size_t)(T < kLayerRankWarps ? T : kLayerRankWarps) * topk_bytes_per_warp(E));
-    L.rk = p; p = align16(p + (size_t)E * 8 + (size_t)kLWarps * 8);  // rank keys, per-warp bounds (one token)
+    L.rk = p; p = align16(p + (size_t)E * 8 + (size_t)kMaxTopK * 8);  // rank keys, picks' lower bounds (one token)
     const size_t phase12 = p - a0;
     // region B: gate/up partials, or the down staging
     const size_t ld = (size_t)I + 8;

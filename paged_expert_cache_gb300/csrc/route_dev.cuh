@@ -462,6 +462,35 @@ __device__ __forceinline__ void sort_desc(unsigned long long (&key)[NPL]) {
 // their bounds, given mx, the largest upper bound (z + b, as a pair) over the
 // experts not picked, and writes the token's ids and weights; where the bounds
 // leave the order open, ranks the token again exactly (topk_token). One warp.
+// Weights of a certified ranking (picks in w.sel / w.selz, rank order), one
+// warp: the softmax over the picks (norm_topk) or over all experts.
+static __device__ __forceinline__ void topk_weights(const CacheDev& c, int t, const TopkSmem& w, int* ids_out,
+                                                    float* wts_out) {
+    const int E = c.E, k = c.k, lane = threadIdx.x & 31;
+    float zref = -INFINITY, sum = 0.f;
+    if (!c.norm_topk) {
+        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    } else {
+        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
+        zref = zj;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        sum = lane < k ? expf(zj - zref) : 0.f;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
+    if (lane < k) {
+        ids_out[t * k + lane] = w.sel[lane];
+        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
+    }
+    __syncwarp();
+}
+
 static __device__ void topk_certify_finish(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
                                            const TopkSmem& w, float2 mx, int* rerank_flag, int* ids_out,
                                            float* wts_out) {
@@ -488,28 +517,7 @@ static __device__ void topk_certify_finish(const CacheDev& c, const Scratch& s, 
         topk_token(c, s, a, t, reinterpret_cast<uint8_t*>(w.z64), rerank_flag, ids_out, wts_out);
         return;
     }
-    float zref = -INFINITY, sum = 0.f;
-    if (!c.norm_topk) {
-        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    } else {
-        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
-        zref = zj;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        sum = lane < k ? expf(zj - zref) : 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    }
-    if (lane < k) {
-        ids_out[t * k + lane] = w.sel[lane];
-        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
-    }
-    __syncwarp();
+    topk_weights(c, t, w, ids_out, wts_out);
 }
 
 // Top-k of token t by one warp, from sorted per-lane lists. Lane l holds the
@@ -593,14 +601,16 @@ static __device__ __forceinline__ void topk_token_fast(const CacheDev& c, const 
 // e builds expert e's key (the orderable 64-bit key of topk_token_fast: the
 // logit's high part, then its low part with 1023 - e in the low bits, so keys
 // are distinct), and its rank is the number of keys above it. Ranks below k
-// are the picks, in the same order as the sorted-list rounds give; the largest
-// upper bound over the rest comes from a block reduction. Warp 0 then
-// certifies and weighs as topk_token_fast does. Every thread of the CTA
-// calls it; keys: E entries and ub: blockDim.x / 32 entries of shared memory.
+// are the picks, in the same order as the sorted-list rounds give. The
+// certificate is topk_token_fast's (each pick's lower bound above the upper
+// bound of everything ranked after it), checked by every expert against the
+// picks above it and combined with one block-wide AND; warp 0 then weighs as
+// topk_token_fast does. Every thread of the CTA calls it; keys: E entries and
+// lowb: k entries of shared memory.
 static __device__ void topk_rank_block(const CacheDev& c, const Scratch& s, const RouteArgs& a, const TopkSmem& w,
-                                       unsigned long long* keys, float2* ub, int* rerank_flag, int* ids_out,
+                                       unsigned long long* keys, float2* lowb, int* rerank_flag, int* ids_out,
                                        float* wts_out) {
-    const int E = c.E, k = c.k, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = c.E, k = c.k, tid = threadIdx.x, warp = tid >> 5;
     float2 z = make_float2(-INFINITY, 0.f);
     float bd = 0.f;
     unsigned long long key = 0ull;
@@ -614,9 +624,11 @@ static __device__ void topk_rank_block(const CacheDev& c, const Scratch& s, cons
         keys[tid] = key;
     }
     __syncthreads();
+    // every expert's upper bound; a pick's lower bound goes to lowb[rank]
     float2 up = make_float2(-INFINITY, 0.f);
+    int rank = E;
     if (tid < E) {
-        int rank = 0;
+        rank = 0;
         const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
 #pragma unroll 4
         for (int i = 0; i < E / 2; ++i) {
@@ -628,25 +640,23 @@ static __device__ void topk_rank_block(const CacheDev& c, const Scratch& s, cons
             w.sel[rank] = tid;
             w.selz[rank] = z;
             w.selb[rank] = bd;
-        } else {
-            up = norm_pair(z.x, __fadd_ru(z.y, bd));
+            lowb[rank] = norm_pair(z.x, __fsub_rd(z.y, bd));
         }
+        up = norm_pair(z.x, __fadd_ru(z.y, bd));
     }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        const float2 o = shfl_pair(up, off);
-        if (pair_gt(o, up)) up = o;
-    }
-    if (lane == 0) ub[warp] = up;
     __syncthreads();
+    // Certified when every pick's lower bound lies above the upper bound of
+    // every expert ranked after it: each expert checks itself against the
+    // picks ranked before it, and the CTA takes the AND.
+    int good = 1;
+    if (tid < E) {
+        const int nj = rank < k ? rank : k;
+        for (int j = 0; j < nj; ++j) good &= pair_gt(lowb[j], up) ? 1 : 0;
+    }
+    const int ok = __syncthreads_and(good);
     if (warp == 0) {
-        float2 mx = lane < (int)(blockDim.x >> 5) ? ub[lane] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float2 o = shfl_pair(mx, off);
-            if (pair_gt(o, mx)) mx = o;
-        }
-        topk_certify_finish(c, s, a, 0, w, mx, rerank_flag, ids_out, wts_out);
+        if (ok) topk_weights(c, 0, w, ids_out, wts_out);
+        else topk_token(c, s, a, 0, reinterpret_cast<uint8_t*>(w.z64), rerank_flag, ids_out, wts_out);
     }
 }
 

@@ -199,6 +199,40 @@ def test_exact_ties_rank_the_lower_expert_first():
     st.close()
 
 
+def test_exact_ties_one_token_on_both_decode_paths():
+    # One token per call: the one-kernel path ranks with one thread per
+    # expert and certifies with a block-wide AND; exact ties fail the
+    # certificate and take the fp64 re-rank. Both paths must pick the lower
+    # expert, match the oracle, and give the same bits.
+    import torch
+    w = scaled(WORKLOADS["tiny"], name="ties1", E=16, k=4, steps=16, streams=(1,), bias=False, slots_per_layer=12)
+    outs = {}
+    for mode in ("one_kernel", "three_kernels"):
+        st = Setup(w, decode=mode)
+        r = st.router[0].copy()
+        r[9] = r[3]
+        r[12] = r[5]
+        r[14] = r[0]
+        st.router[0] = r
+        st.router_dev[0] = torch.from_numpy(r.view(np.int16)).to(st.dev)
+        orc = OracleRun(w, st.info["slot_bytes"])
+        xs = st.hiddens(0, 1, w.steps)
+        ys = []
+        for step in range(w.steps):
+            ys.append(st.forward(xs[step], 0))
+            ids, _ = orc.route(xs[step], st.router[0], st.bias)
+            plan = orc.plan(0, ids, 1)
+            compare_trace(st.cache.trace_read()[0], ids, plan, 0, 1)
+            _, _, yo = orc.layer(xs[step], st.router[0], st.bias, 0)
+            assert rel_l2(ys[-1], yo) <= TOL
+        info = st.cache.info()
+        assert info["fused_decode_calls" if mode == "one_kernel" else "split_decode_calls"] == w.steps
+        assert st.cache.stats()["topk_fp64_rerank"] > 0
+        outs[mode] = np.stack(ys)
+        st.close()
+    assert np.array_equal(outs["one_kernel"], outs["three_kernels"])
+
+
 @pytest.mark.parametrize("fmt,pool_mode,E,T", [
     ("q4_0", "per_layer", 64, 1), ("q4_0", "shared", 64, 3), ("fp8_b128", "per_layer", 40, 8),
     ("nvfp4", "shared", 160, 2), ("bf16", "per_layer", 16, 4), ("nvfp4", "per_layer", 160, 4)])
