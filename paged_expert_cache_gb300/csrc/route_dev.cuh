@@ -314,6 +314,33 @@ __device__ inline TopkSmem topk_layout(uint8_t* base, int E) {
     return t;
 }
 
+// Weights of a ranking (picks in w.sel / w.selz, rank order), one warp: the
+// softmax over the picks (norm_topk) or over all experts. Every ranking path
+// ends here, so a token's weights do not depend on the path that ranked it.
+static __device__ __forceinline__ void topk_weights(const CacheDev& c, int t, const TopkSmem& w, int* ids_out,
+                                                    float* wts_out) {
+    const int E = c.E, k = c.k, lane = threadIdx.x & 31;
+    float zref = -INFINITY, sum = 0.f;
+    if (!c.norm_topk) {
+        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
+        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    } else {
+        // every lane takes the picks' largest logit and sums their
+        // exponentials in rank order: k reads, no cross-lane steps
+        for (int j = 0; j < k; ++j) zref = fmaxf(zref, w.selz[j].x);
+        for (int j = 0; j < k; ++j) sum += expf(w.selz[j].x - zref);
+    }
+    if (lane < k) {
+        ids_out[t * k + lane] = w.sel[lane];
+        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
+    }
+    __syncwarp();
+}
+
 // Top-k of token t by one warp; writes ids and weights of the token.
 // The scratch comes as its base address (topk_layout's), not as a TopkSmem:
 // a reference would put the caller's TopkSmem in local memory, and every
@@ -410,30 +437,7 @@ static __device__ __noinline__ void topk_token(const CacheDev& c, const Scratch&
         if (lane == 0) *rerank_flag = 1;
     }
     __syncwarp();
-    // combine weights in fp32 from the picks' logits
-    float zref = -INFINITY, sum = 0.f;
-    if (!c.norm_topk) {
-        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    } else {
-        // the register ranking's order: pick j on lane j, then a butterfly
-        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
-        zref = zj;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        sum = lane < k ? expf(zj - zref) : 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    }
-    if (lane < k) {
-        ids_out[t * k + lane] = w.sel[lane];
-        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
-    }
-    __syncwarp();
+    topk_weights(c, t, w, ids_out, wts_out);
 }
 
 // Descending bitonic sorting network over NPL (a power of two) keys held in
@@ -462,35 +466,6 @@ __device__ __forceinline__ void sort_desc(unsigned long long (&key)[NPL]) {
 // their bounds, given mx, the largest upper bound (z + b, as a pair) over the
 // experts not picked, and writes the token's ids and weights; where the bounds
 // leave the order open, ranks the token again exactly (topk_token). One warp.
-// Weights of a certified ranking (picks in w.sel / w.selz, rank order), one
-// warp: the softmax over the picks (norm_topk) or over all experts.
-static __device__ __forceinline__ void topk_weights(const CacheDev& c, int t, const TopkSmem& w, int* ids_out,
-                                                    float* wts_out) {
-    const int E = c.E, k = c.k, lane = threadIdx.x & 31;
-    float zref = -INFINITY, sum = 0.f;
-    if (!c.norm_topk) {
-        for (int e = lane; e < E; e += 32) zref = fmaxf(zref, w.z[e].x);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        for (int e = lane; e < E; e += 32) sum += expf(w.z[e].x - zref);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    } else {
-        const float zj = lane < k ? w.selz[lane].x : -INFINITY;
-        zref = zj;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) zref = fmaxf(zref, __shfl_xor_sync(0xffffffffu, zref, off));
-        sum = lane < k ? expf(zj - zref) : 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    }
-    if (lane < k) {
-        ids_out[t * k + lane] = w.sel[lane];
-        wts_out[t * k + lane] = expf(w.selz[lane].x - zref) / sum;
-    }
-    __syncwarp();
-}
-
 static __device__ void topk_certify_finish(const CacheDev& c, const Scratch& s, const RouteArgs& a, int t,
                                            const TopkSmem& w, float2 mx, int* rerank_flag, int* ids_out,
                                            float* wts_out) {
