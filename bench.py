@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
     ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
-                    help="decode launch mode (auto: one kernel for single-token calls on per-layer pools)")
+                    help="decode launch mode (auto: one kernel for one- or two-token calls on per-layer pools)")
     ap.add_argument("--prefill", action="store_true",
                     help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()

@@ -422,12 +422,14 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     // events bracket each launch for profiling)
     const bool pdl = !h->prof_on;
     bool fused = false;
-    // MOE_DECODE_AUTO takes the one-kernel path for single-token calls on per-layer
-    // pools: measured interleaved on one GPU it is 1-6% faster there, and 2-6%
-    // slower with two tokens or with one pool shared by every layer, where each
-    // CTA's redundant ranking and plan cost more than the kernel boundaries saved
+    // MOE_DECODE_AUTO takes the one-kernel path for calls of one or two tokens on
+    // per-layer pools: measured interleaved on one GPU it is 3-14% faster there
+    // (equal for two Q4_0 tokens), and slower with four tokens or with one pool
+    // shared by every layer, where each CTA's redundant ranking and plan, and
+    // one CTA per SM streaming more units, cost more than the kernel
+    // boundaries saved
     const int mode = h->cfg.split_decode;
-    const bool one_kernel_pays = mode == MOE_DECODE_ONE_KERNEL || (T == 1 && d.pool_mode == MOE_POOL_PER_LAYER);
+    const bool one_kernel_pays = mode == MOE_DECODE_ONE_KERNEL || (T <= 2 && d.pool_mode == MOE_POOL_PER_LAYER);
     if (decode && mode != MOE_DECODE_THREE_KERNELS && one_kernel_pays && h->fused_ok &&
         h->cfg.upload_mode == MOE_UPLOAD_PULL && moe::layer_smem_bytes(d, T) > 0) {
         // the whole call in one persistent kernel

@@ -302,16 +302,16 @@ def one_vs_three_kernels(fmt, pool_mode, E, T, k, H, I, L, steps, has_shared):
 
 
 def test_decode_modes_choose_their_path_and_agree():
-    # AUTO takes one kernel for a single token on per-layer pools and three
-    # kernels for two tokens; ONE_KERNEL and THREE_KERNELS force the path.
-    # Every mode gives the same bits.
-    w = scaled(WORKLOADS["qwen3_30b_a3b_q4_0"], name="modes", L=2, E=32, k=4, H=512, I=192, slots_per_layer=12,
-               streams=(2,), steps=3, rho=0.7)
+    # AUTO takes one kernel for one or two tokens on per-layer pools and three
+    # kernels for three; ONE_KERNEL and THREE_KERNELS force the path. Every
+    # mode gives the same bits.
+    w = scaled(WORKLOADS["qwen3_30b_a3b_q4_0"], name="modes", L=2, E=32, k=4, H=512, I=192, slots_per_layer=16,
+               streams=(3,), steps=3, rho=0.7)
     outs = {}
     for mode in ("auto", "one_kernel", "three_kernels"):
         st = Setup(w, decode=mode)
         ys = []
-        for T in (1, 2):
+        for T in (1, 2, 3):
             xs = {l: st.hiddens(l, T, w.steps) for l in range(w.L)}
             for s in range(w.steps):
                 for l in range(w.L):
@@ -320,8 +320,8 @@ def test_decode_modes_choose_their_path_and_agree():
         outs[mode] = (np.concatenate([y.reshape(-1) for y in ys]), info["fused_decode_calls"], info["split_decode_calls"])
         st.close()
     per_T = w.steps * w.L
-    assert outs["auto"][1:] == (per_T, per_T)
-    assert outs["one_kernel"][1:] == (2 * per_T, 0)
-    assert outs["three_kernels"][1:] == (0, 2 * per_T)
+    assert outs["auto"][1:] == (2 * per_T, per_T)
+    assert outs["one_kernel"][1:] == (3 * per_T, 0)
+    assert outs["three_kernels"][1:] == (0, 3 * per_T)
     assert np.array_equal(outs["auto"][0], outs["one_kernel"][0])
     assert np.array_equal(outs["auto"][0], outs["three_kernels"][0])
