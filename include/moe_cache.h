@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -120,11 +120,15 @@ typedef struct {
     int32_t device;           /* CUDA device ordinal */
     int32_t split_decode;     /* moe_decode_mode_t: how decode calls are launched (default
                                  MOE_DECODE_AUTO). Every mode gives bitwise identical results. */
+    int32_t multi_wave;       /* 0 (default): a decode call with T * top_k above its pool's slots
+                                 fails with MOE_ERR_CAPACITY. 1: it runs as successive waves of
+                                 floor(slots / top_k) tokens (the last one shorter), each a cache
+                                 transaction and a trace record of its own, in token order. */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
- * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO; shape fields
- * zero. */
+ * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0;
+ * shape fields zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {
@@ -208,8 +212,11 @@ moe_status_t moe_cache_load_shared(moe_cache_t* h, int32_t layer, const void* re
  * MOE_ERR_INVALID for a bad layer, T <= 0 or T > max_tokens, null pointers;
  * MOE_ERR_CAPACITY when T * top_k exceeds the layer's pool on the decode path
  * (the single-wave rule of [PAGED, "What happens with more than one
- * request?"]); MOE_ERR_STATE if experts were never loaded; MOE_ERR_CUDA if a
- * launch fails. In MOE_UPLOAD_MEMCPY mode the call synchronises `stream`. */
+ * request?"]) and multi_wave is 0; with multi_wave 1 such a call runs as
+ * waves of floor(slots / top_k) tokens, each with its own page-in, as that
+ * section describes for batches past the rule. MOE_ERR_STATE if experts were
+ * never loaded; MOE_ERR_CUDA if a launch fails. In MOE_UPLOAD_MEMCPY mode the
+ * call synchronises `stream`. */
 moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, const void* router_w,
                                const float* router_bias, int32_t layer_id, float* out, void* stream);
 

@@ -73,6 +73,7 @@ def lib():
         L.orc_cache_slots.argtypes = [vp]
         L.orc_cache_stats.argtypes = [vp, vp]
         L.orc_count_runs.argtypes = [vp, vp, i32]
+        L.orc_wave_split.argtypes = [i32, i32, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -175,6 +176,14 @@ def count_runs(fill_expert, fill_slot):
     fe = np.ascontiguousarray(fill_expert, dtype=np.int32)
     fs = np.ascontiguousarray(fill_slot, dtype=np.int32)
     return int(lib().orc_count_runs(fe.ctypes.data, fs.ctypes.data, fe.size))
+
+
+def wave_split(T, k, K):
+    """[(first token, tokens)] of each wave of a decode step (moe_oracle.c)."""
+    start = np.empty(max(T, 1), dtype=np.int32)
+    count = np.empty(max(T, 1), dtype=np.int32)
+    n = int(lib().orc_wave_split(T, k, K, start.ctypes.data, count.ctypes.data))
+    return [(int(start[i]), int(count[i])) for i in range(n)]
 
 
 class CacheError(RuntimeError):

@@ -582,6 +582,25 @@ void orc_cache_stats(const orc_cache* c, uint64_t* stats) {
         for (j = 0; j < 4; ++j) stats[b * 4 + j] = c->stats[b][j];
 }
 
+/* Waves of a decode step [PAGED, "What happens with more than one request?"]:
+ * a step is served by one wave only if tokens x top_k <= K, that is up to
+ * K // top_k tokens; a larger step needs several waves, each with its own
+ * page-in. The page does not say how the tokens are grouped; the plainest
+ * reading, taken here, is successive groups of K // top_k tokens in token
+ * order, the last one shorter. Writes each wave's first token and token
+ * count; returns the number of waves, or 0 when K < top_k (no wave fits). */
+int orc_wave_split(int T, int k, int K, int32_t* start, int32_t* count) {
+    int per, n = 0, t0;
+    if (T < 1 || k < 1 || K < k) return 0;
+    per = K / k;
+    for (t0 = 0; t0 < T; t0 += per) {
+        start[n] = t0;
+        count[n] = (T - t0 < per) ? T - t0 : per;
+        n++;
+    }
+    return n;
+}
+
 /* Consecutive experts going to consecutive slots move as one copy
  * [EXPLAINER, "Inside llama.cpp PR #29887"]. */
 int orc_count_runs(const int32_t* fill_expert, const int32_t* fill_slot, int n_fill) {

@@ -114,6 +114,9 @@ int orc_cache_num_pools(const orc_cache* c);
 int orc_cache_slots(const orc_cache* c);
 /* stats[bucket*4 + {0 calls, 1 hits, 2 misses, 3 bytes}], buckets: T<=8, 9..32, >32. */
 void orc_cache_stats(const orc_cache* c, uint64_t* stats);
+/* The waves of a decode step of T tokens on a pool of K slots: successive
+ * groups of K // k tokens; returns their number (0 if K < k). */
+int orc_wave_split(int T, int k, int K, int32_t* start, int32_t* count);
 /* Number of copies after merging runs where expert and slot both step by one. */
 int orc_count_runs(const int32_t* fill_expert, const int32_t* fill_slot, int n_fill);
 

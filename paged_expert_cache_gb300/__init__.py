@@ -31,7 +31,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("num_layers", i32), ("num_experts", i32), ("top_k", i32), ("hidden", i32), ("inter", i32),
                 ("format", i32), ("has_shared", i32), ("pool_mode", i32), ("slots_per_layer", i32),
                 ("upload_mode", i32), ("pool_bytes", dbl), ("norm_topk", i32), ("max_cache_tokens", i32),
-                ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32)]
+                ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32),
+                ("multi_wave", i32)]
 
 
 class BucketStats(ctypes.Structure):
@@ -122,7 +123,7 @@ def _check(st, handle=None):
 
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
-                max_tokens=32, device=0, decode="auto"):
+                max_tokens=32, device=0, decode="auto", multi_wave=False):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -138,6 +139,7 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.max_tokens = max_tokens
     c.device = device
     c.split_decode = DECODE_MODES[decode] if isinstance(decode, str) else int(decode)
+    c.multi_wave = 1 if multi_wave else 0
     return c
 
 

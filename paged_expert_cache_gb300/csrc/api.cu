@@ -152,6 +152,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->max_tokens = 32;
     cfg->device = 0;
     cfg->split_decode = MOE_DECODE_AUTO;
+    cfg->multi_wave = 0;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -181,6 +182,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         return fail(nullptr, MOE_ERR_INVALID, "unknown upload_mode");
     if (c.split_decode < MOE_DECODE_AUTO || c.split_decode > MOE_DECODE_ONE_KERNEL)
         return fail(nullptr, MOE_ERR_INVALID, "unknown decode mode (split_decode)");
+    if (c.multi_wave != 0 && c.multi_wave != 1) return fail(nullptr, MOE_ERR_INVALID, "multi_wave must be 0 or 1");
     if (c.max_cache_tokens < 1 || c.max_cache_tokens > moe::kDecodeMaxTokens)
         return fail(nullptr, MOE_ERR_INVALID, "max_cache_tokens must be in 1..32");
     if (c.max_tokens < 1) return fail(nullptr, MOE_ERR_INVALID, "max_tokens must be >= 1");
@@ -400,8 +402,21 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         return fail(h, MOE_ERR_STATE, "experts not loaded");
     cudaStream_t st = (cudaStream_t)stream;
     const bool decode = T <= h->cfg.max_cache_tokens;
-    if (decode && (int64_t)T * d.k > d.K)
-        return fail(h, MOE_ERR_CAPACITY, "tokens * top_k exceeds the slots of this layer's pool");
+    if (decode && (int64_t)T * d.k > d.K) {
+        if (!h->cfg.multi_wave)
+            return fail(h, MOE_ERR_CAPACITY, "tokens * top_k exceeds the slots of this layer's pool");
+        // Several waves, each within the single-wave rule: floor(K / k) tokens
+        // per wave (at least one, since create requires K >= k), in token
+        // order, each its own cache transaction.
+        const int per_wave = d.K / d.k;
+        for (int t0 = 0; t0 < T; t0 += per_wave) {
+            const int tw = std::min(per_wave, T - t0);
+            const moe_status_t r = moe_layer_forward(h, (const uint16_t*)hidden + (size_t)t0 * d.H, tw, router_w,
+                                                     router_bias, layer_id, out + (size_t)t0 * d.H, stream);
+            if (r != MOE_OK) return r;
+        }
+        return MOE_OK;
+    }
     const int bucket = T <= 8 ? 0 : (T <= 32 ? 1 : 2);
     moe::RouteArgs a;
     a.x = (const uint16_t*)hidden;

@@ -31,7 +31,8 @@ def pool_slots(w, slot_bytes, K=None):
 class Setup:
     """A GPU cache plus the workload's device inputs."""
 
-    def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto"):
+    def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
+                 multi_wave=False):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -40,7 +41,7 @@ class Setup:
                               slots_per_layer=(K if K is not None else w.slots_per_layer),
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
-                              decode=decode)
+                              decode=decode, multi_wave=multi_wave)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):

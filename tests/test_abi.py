@@ -13,7 +13,7 @@ def test_library_exports_every_header_function():
     assert "moe_layer_forward" in names and "moe_cache_create" in names and "moe_cache_stats" in names
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 def test_config_defaults():
@@ -22,6 +22,7 @@ def test_config_defaults():
     assert c.norm_topk == 1 and c.max_cache_tokens == 32 and c.prefill_group == 32 and c.max_tokens == 32
     assert c.upload_mode == 0 and c.pool_mode == 0
     assert c.split_decode == 0  # automatic choice of the decode launch
+    assert c.multi_wave == 0  # single-wave rule: over-capacity decode calls are refused
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -44,3 +45,11 @@ def test_invalid_configurations_are_refused(kw, status):
         pec.MoECache(cfg)
     assert ei.value.status == status
     assert str(ei.value)
+
+
+def test_multi_wave_flag_must_be_0_or_1():
+    cfg = pec.make_config(1, 16, 2, 256, 128, slots_per_layer=8)
+    cfg.multi_wave = 2
+    with pytest.raises(pec.MoeError) as ei:
+        pec.MoECache(cfg)
+    assert ei.value.status == pec.ERR_INVALID

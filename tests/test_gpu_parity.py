@@ -199,6 +199,48 @@ def test_exact_ties_rank_the_lower_expert_first():
     st.close()
 
 
+@pytest.mark.parametrize("pool_mode", ["per_layer", "shared"])
+def test_multi_wave_decode_matches_the_oracle_wave_by_wave(pool_mode):
+    # T * k above the pool's slots with multi_wave: waves of K // k tokens in
+    # token order, each its own cache transaction and trace record, checked
+    # against the oracle's wave split and literal LRU; the outputs match the
+    # unpaged layer and, bit for bit, a pool large enough for one wave.
+    import oracle
+    T, K = 7, 10
+    w = scaled(WORKLOADS["tiny"], name="waves", L=2, E=16, k=4, steps=5, streams=(T,), bias=True,
+               pool_mode=pool_mode, slots_per_layer=K, pool_bytes=0.0)
+    sb = oracle.slot_bytes(w.fmt, w.H, w.I)
+    if pool_mode == "shared":
+        w = scaled(w, pool_bytes=sb * K + 5)
+    waves = oracle.wave_split(T, w.k, K)
+    assert len(waves) == 4
+    outs = []
+    for big in (False, True):
+        st = Setup(w, multi_wave=True, max_tokens=T, K=(4 * K if big else None),
+                   pool_bytes=(sb * 4 * K if big and pool_mode == "shared" else None))
+        orc = OracleRun(w, st.info["slot_bytes"])
+        xs = {l: st.hiddens(l, T, w.steps) for l in range(w.L)}
+        ys = []
+        for step in range(w.steps):
+            for l in range(w.L):
+                x = xs[l][step]
+                y = st.forward(x, l)
+                ys.append(y)
+                recs = st.cache.trace_read()
+                if big:
+                    assert len(recs) == 1
+                    continue
+                assert len(recs) == len(waves)
+                for rec, (s0, n) in zip(recs, waves):
+                    ids, _ = orc.route(x[s0:s0 + n], st.router[l], st.bias)
+                    compare_trace(rec, ids, orc.plan(l, ids, n), l, n)
+                _, _, yo = orc.layer(x, st.router[l], st.bias, l)
+                assert rel_l2(y, yo) <= TOL
+        outs.append(np.stack(ys))
+        st.close()
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_exact_ties_one_token_on_both_decode_paths():
     # One token per call: the one-kernel path ranks with one thread per
     # expert and certifies with a block-wide AND; exact ties fail the
