@@ -378,6 +378,9 @@ struct orc_cache {
     char* seen;      /* [E] scratch */
     int32_t* uniq;   /* [E] scratch */
     char* was_hit;   /* [E] scratch */
+    int policy;      /* ORC_POLICY_LRU or ORC_POLICY_LFU */
+    uint64_t* uses;  /* [L*E] calls that routed each key, over the whole history (LFU) */
+    char* inuse;     /* [K] scratch: slots the current call holds (LFU) */
 };
 
 /* Initial list: every slot empty, ordered 0..K-1 with slot 0 at the head. */
@@ -396,6 +399,7 @@ void orc_cache_reset(orc_cache* c) {
         c->tail[p] = c->K - 1;
     }
     memset(c->stats, 0, sizeof(c->stats));
+    memset(c->uses, 0, sizeof(uint64_t) * (size_t)c->L * c->E);
 }
 
 orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, double slot_bytes,
@@ -420,8 +424,29 @@ orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, dou
     c->seen = (char*)malloc((size_t)E);
     c->uniq = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
     c->was_hit = (char*)malloc((size_t)E);
+    c->uses = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)L * E);
+    c->inuse = (char*)malloc((size_t)c->K);
+    c->policy = ORC_POLICY_LRU;
     orc_cache_reset(c);
     return c;
+}
+
+/* Eviction policy. LRU is the page's [EXPLAINER, "Inside llama.cpp PR
+ * #29887"]. LFU is the frequency policy of [EXPLAINER, "How MoE expert
+ * offloading works with an LRU expert cache"] (its toy table's LFU column)
+ * and [FP4LOCAL, "Decode"] ("least frequently used eviction"); neither page
+ * prints its rule. Reading taken: every key counts the calls that routed it
+ * over the whole history (evicted or not); a miss takes, among the slots the
+ * call does not hold, the one whose key has the fewest uses (an empty slot
+ * first), the least recently used on ties. Counting over the whole history
+ * is what makes the toy's LFU hit rate the probability mass of its most
+ * popular experts, as its column shows. Changing the policy resets the
+ * cache. */
+int orc_cache_set_policy(orc_cache* c, int policy) {
+    if (!c || (policy != ORC_POLICY_LRU && policy != ORC_POLICY_LFU)) return ORC_ERR_INVALID;
+    c->policy = policy;
+    orc_cache_reset(c);
+    return ORC_OK;
 }
 
 void orc_cache_destroy(orc_cache* c) {
@@ -435,6 +460,8 @@ void orc_cache_destroy(orc_cache* c) {
     free(c->seen);
     free(c->uniq);
     free(c->was_hit);
+    free(c->uses);
+    free(c->inuse);
     free(c);
 }
 
@@ -519,10 +546,15 @@ int orc_cache_plan(orc_cache* c, int layer, const int32_t* ids, int n_ids, int T
 
     if (nu > c->K) return ORC_ERR_CAPACITY;
 
+    if (c->policy == ORC_POLICY_LFU) {
+        memset(c->inuse, 0, (size_t)c->K);
+        for (i = 0; i < nu; ++i) c->uses[(size_t)layer * c->E + c->uniq[i]] += 1;
+    }
     for (i = 0; i < nu; ++i) {
         int32_t e = c->uniq[i];
         if (smap[e] >= 0) {
             lru_touch(c, p, smap[e]);
+            if (c->policy == ORC_POLICY_LFU) c->inuse[smap[e]] = 1;
             c->was_hit[e] = 1;
             nh++;
         }
@@ -533,6 +565,22 @@ int orc_cache_plan(orc_cache* c, int layer, const int32_t* ids, int n_ids, int T
         int32_t s, old;
         if (c->was_hit[e]) continue;
         s = c->head[p];
+        if (c->policy == ORC_POLICY_LFU) {
+            /* walk the list from its least recent end; keep the first slot
+             * with the fewest uses among those the call does not hold */
+            int32_t q = c->head[p], best = -1;
+            double best_uses = 0.0;
+            while (q >= 0) {
+                if (!c->inuse[q]) {
+                    const int32_t key = c->key_of[(size_t)p * c->K + q];
+                    const double u = key < 0 ? -1.0 : (double)c->uses[key];
+                    if (best < 0 || u < best_uses) { best = q; best_uses = u; }
+                }
+                q = c->next[(size_t)p * c->K + q];
+            }
+            s = best;
+            c->inuse[s] = 1;
+        }
         old = c->key_of[(size_t)p * c->K + s];
         if (old >= 0) c->slot_map[old] = -1; /* key = layer*E + expert */
         c->key_of[(size_t)p * c->K + s] = layer * c->E + e;

@@ -44,6 +44,7 @@ extern "C" {
 enum { ORC_FMT_BF16 = 0, ORC_FMT_Q4_0 = 1, ORC_FMT_FP8_B128 = 2, ORC_FMT_NVFP4 = 3 };
 /* Pool scopes: one K-slot pool per layer [PAGED], or one pool for all layers [T4]. */
 enum { ORC_POOL_PER_LAYER = 0, ORC_POOL_SHARED = 1 };
+enum { ORC_POLICY_LRU = 0, ORC_POLICY_LFU = 1 };
 /* Status codes. */
 enum { ORC_OK = 0, ORC_ERR_INVALID = 1, ORC_ERR_CAPACITY = 2, ORC_ERR_MISSING = 3 };
 
@@ -114,6 +115,9 @@ int orc_cache_num_pools(const orc_cache* c);
 int orc_cache_slots(const orc_cache* c);
 /* stats[bucket*4 + {0 calls, 1 hits, 2 misses, 3 bytes}], buckets: T<=8, 9..32, >32. */
 void orc_cache_stats(const orc_cache* c, uint64_t* stats);
+/* Eviction policy (ORC_POLICY_LRU, the default, or ORC_POLICY_LFU); resets the
+ * cache. ORC_ERR_INVALID for another value. */
+int orc_cache_set_policy(orc_cache* c, int policy);
 /* The waves of a decode step of T tokens on a pool of K slots: successive
  * groups of K // k tokens; returns their number (0 if K < k). */
 int orc_wave_split(int T, int k, int K, int32_t* start, int32_t* count);
