@@ -101,6 +101,18 @@ typedef enum {
     MOE_DECODE_ONE_KERNEL = 2     /* one kernel for every call that fits */
 } moe_decode_mode_t;
 
+/* Which slot a miss takes. LRU: the least recently used slot not held by the
+ * call [EXPLAINER, "Inside llama.cpp PR #29887"]. LFU: a least frequently
+ * used policy [FP4LOCAL, "Decode"]; the pages print no rule, so: every
+ * (layer, expert) counts the decode calls that routed it over the whole
+ * history, and a miss takes, among the slots its call does not hold, an empty
+ * slot first, else the one whose expert has the fewest such calls, the least
+ * recently used on ties. Counts saturate at 2^23. */
+typedef enum {
+    MOE_EVICT_LRU = 0,
+    MOE_EVICT_LFU = 1
+} moe_eviction_t;
+
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_experts;      /* E routed experts per layer, 1..1024 */
@@ -124,11 +136,12 @@ typedef struct {
                                  fails with MOE_ERR_CAPACITY. 1: it runs as successive waves of
                                  floor(slots / top_k) tokens (the last one shorter), each a cache
                                  transaction and a trace record of its own, in token order. */
+    int32_t eviction;         /* moe_eviction_t (default MOE_EVICT_LRU) */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
- * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0;
- * shape fields zero. */
+ * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0,
+ * MOE_EVICT_LRU; shape fields zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {

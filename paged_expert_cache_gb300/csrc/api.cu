@@ -126,6 +126,7 @@ moe_status_t init_tables(moe_cache_t* h) {
     CK(h, cudaMemcpy(d.last_use, lu.data(), lu.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.clock, clk.data(), clk.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
     CK(h, cudaMemset(d.stats, 0, 16 * sizeof(unsigned long long)));
+    CK(h, cudaMemset(d.uses, 0, (size_t)d.L * d.E * sizeof(unsigned)));
     if (h->scr.grid_bar) CK(h, cudaMemset(h->scr.grid_bar, 0, sizeof(unsigned)));
     if (h->scr.err) CK(h, cudaMemset(h->scr.err, 0, sizeof(unsigned)));
     if (h->scr.logit_ctr) CK(h, cudaMemset(h->scr.logit_ctr, 0, 2 * sizeof(unsigned)));
@@ -153,6 +154,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->device = 0;
     cfg->split_decode = MOE_DECODE_AUTO;
     cfg->multi_wave = 0;
+    cfg->eviction = MOE_EVICT_LRU;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -183,6 +185,8 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     if (c.split_decode < MOE_DECODE_AUTO || c.split_decode > MOE_DECODE_ONE_KERNEL)
         return fail(nullptr, MOE_ERR_INVALID, "unknown decode mode (split_decode)");
     if (c.multi_wave != 0 && c.multi_wave != 1) return fail(nullptr, MOE_ERR_INVALID, "multi_wave must be 0 or 1");
+    if (c.eviction != MOE_EVICT_LRU && c.eviction != MOE_EVICT_LFU)
+        return fail(nullptr, MOE_ERR_INVALID, "unknown eviction policy");
     if (c.max_cache_tokens < 1 || c.max_cache_tokens > moe::kDecodeMaxTokens)
         return fail(nullptr, MOE_ERR_INVALID, "max_cache_tokens must be in 1..32");
     if (c.max_tokens < 1) return fail(nullptr, MOE_ERR_INVALID, "max_tokens must be >= 1");
@@ -265,6 +269,8 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(d.key_of, (size_t)d.n_pools * d.K);
     DA(d.last_use, (size_t)d.n_pools * d.K);
     DA(d.clock, (size_t)d.n_pools);
+    DA(d.uses, (size_t)d.L * d.E);
+    d.lfu = c.eviction == MOE_EVICT_LFU ? 1 : 0;
     DA(d.stats, 16);
     DA(d.trace_count, 1);
     d.trace = nullptr;

@@ -117,6 +117,8 @@ struct CacheDev {
     int* key_of;                 // [n_pools*K]
     unsigned long long* last_use;  // [n_pools*K] clock of the last use
     unsigned long long* clock;     // [n_pools]
+    unsigned* uses;                // [L*E] decode calls that routed each key (LFU)
+    int lfu;                       // 1: least frequently used eviction
     unsigned long long* stats;     // [3][5] + [15] re-rank count
     int* trace;                    // ring of records, or null
     unsigned long long* trace_count;

@@ -740,6 +740,30 @@ static __device__ void plan_prefetch(const CacheDev& c, const RouteArgs& a, cons
     for (int i = tid; i <= c.E / 32; i += nthr) m.missbits[i] = 0u;
 }
 
+// LFU victim order (eviction MOE_EVICT_LFU): the staged last-use stamps are
+// replaced in shared memory by 64-bit keys, (uses of the slot's key + 1, or 0
+// for an empty slot) above the stamp's low 40 bits, so the smallest keys are
+// empty slots first, then the fewest uses, then the least recent. The slots
+// this call holds (stamped from clk on) become ~0 and are never chosen.
+constexpr unsigned kLfuUseCap = 1u << 23;
+__device__ __forceinline__ void lfu_victim_keys(const CacheDev& c, const PlanSmem& m, unsigned long long clk) {
+    for (int i = threadIdx.x; i < c.K; i += blockDim.x) {
+        const unsigned long long st = m.lu[i];
+        if (st >= clk) {
+            m.lu[i] = ~0ull;
+            continue;
+        }
+        const int key = m.kof[i];
+        unsigned long long u = 0ull;
+        if (key >= 0) {
+            const unsigned n = c.uses[key];
+            u = (unsigned long long)(n < kLfuUseCap ? n : kLfuUseCap) + 1ull;
+        }
+        m.lu[i] = (u << 40) | (st & ((1ull << 40) - 1ull));
+    }
+    __syncthreads();
+}
+
 // ids_in: the call's picks ([T][k]). The descriptors go to units_out
 // (global for the expert kernels, or the CTA's shared memory when every CTA
 // plans for itself). Only a committing CTA writes the pool's state, the fill
@@ -778,6 +802,9 @@ static __device__ void plan_decode(const CacheDev& c, const Scratch& s, const Ro
         }
         __syncwarp();
         const int nu = base;
+        // every expert of the call counts one more use (LFU)
+        if (commit && c.lfu)
+            for (int u = tid; u < nu; u += 32) c.uses[(size_t)layer * E + m.u_expert[u]] += 1u;
         // 2. hits, touched in unit order: stamps clock + hit rank
         int hb = 0;
         for (int u0 = 0; u0 < nu; u0 += 32) {
@@ -828,7 +855,8 @@ static __device__ void plan_decode(const CacheDev& c, const Scratch& s, const Ro
     const int nu = m.scal[0];
     const int nh = m.scal[1];
     const int nmiss = nu - nh;
-    // 3. victims: the nmiss smallest stamps of the pool, smallest first
+    if (c.lfu && nmiss > 0) lfu_victim_keys(c, m, clk);
+    // 3. victims: the nmiss smallest stamps of the pool (LFU: keys), smallest first
     if (nmiss > 0) {
         unsigned long long myv = ~0ull;
         int mys = -1;
@@ -1016,6 +1044,9 @@ static __device__ __forceinline__ void plan_small(const CacheDev& c, const Scrat
             nu += __popc(bal);
         }
         __syncwarp();
+        // every expert of the call counts one more use (LFU)
+        if (commit && c.lfu)
+            for (int u = lane; u < nu; u += 32) c.uses[(size_t)layer * E + m.u_expert[u]] += 1u;
         // 2. hits, touched in unit order: stamps clock + hit rank
         int nh = 0;
         for (int u0 = 0; u0 < nu; u0 += 32) {
@@ -1066,7 +1097,8 @@ static __device__ __forceinline__ void plan_small(const CacheDev& c, const Scrat
     const int nu = m.scal[0];
     const int nh = m.scal[1];
     const int nmiss = nu - nh;
-    // 3. victims: the nmiss smallest stamps of the pool, smallest first
+    if (c.lfu && nmiss > 0) lfu_victim_keys(c, m, clk);
+    // 3. victims: the nmiss smallest stamps of the pool (LFU: keys), smallest first
     if (nmiss > 0) {
         unsigned long long myv = ~0ull;
         int mys = -1;

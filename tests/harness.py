@@ -32,7 +32,7 @@ class Setup:
     """A GPU cache plus the workload's device inputs."""
 
     def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
-                 multi_wave=False):
+                 multi_wave=False, eviction="lru"):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -41,7 +41,7 @@ class Setup:
                               slots_per_layer=(K if K is not None else w.slots_per_layer),
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
-                              decode=decode, multi_wave=multi_wave)
+                              decode=decode, multi_wave=multi_wave, eviction=eviction)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):
@@ -80,10 +80,10 @@ class Setup:
 class OracleRun:
     """The same calls through the oracle: routing, literal LRU, unpaged layer."""
 
-    def __init__(self, w, slot_bytes, K=None):
+    def __init__(self, w, slot_bytes, K=None, policy="lru"):
         self.w = w
         self.K = pool_slots(w, slot_bytes, K)
-        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes)
+        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy)
         self._rec = {}
 
     def record(self, layer, e):

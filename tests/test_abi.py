@@ -23,6 +23,7 @@ def test_config_defaults():
     assert c.upload_mode == 0 and c.pool_mode == 0
     assert c.split_decode == 0  # automatic choice of the decode launch
     assert c.multi_wave == 0  # single-wave rule: over-capacity decode calls are refused
+    assert c.eviction == 0  # least recently used
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -36,6 +37,7 @@ def test_config_defaults():
     (dict(L=1, E=16, k=2, H=256, I=128, pool_mode="shared", pool_bytes=196608 * 2 - 1), pec.ERR_CAPACITY),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, max_cache_tokens=33), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, decode=3), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, eviction=2), pec.ERR_INVALID),
 ])
 def test_invalid_configurations_are_refused(kw, status):
     args = dict(kw)

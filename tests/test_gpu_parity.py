@@ -241,6 +241,42 @@ def test_multi_wave_decode_matches_the_oracle_wave_by_wave(pool_mode):
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("pool_mode", ["per_layer", "shared"])
+def test_lfu_eviction_matches_the_oracle_on_both_decode_paths(pool_mode):
+    # eviction LFU: every call's routing, slots, hits and fills bit-exact
+    # against the oracle's LFU, on the one-kernel and the three-kernel paths
+    # (which agree bit for bit), with a pool small enough to evict often; the
+    # policy must also part from LRU somewhere on the way.
+    import oracle
+    w = scaled(WORKLOADS["tiny"], name="lfu", L=2, E=16, k=2, steps=24, streams=(2,), bias=True,
+               pool_mode=pool_mode, slots_per_layer=5, pool_bytes=0.0, rho=0.5)
+    if pool_mode == "shared":
+        w = scaled(w, pool_bytes=oracle.slot_bytes(w.fmt, w.H, w.I) * 7 + 5)
+    runs = {}
+    for decode in ("one_kernel", "three_kernels"):
+        st = Setup(w, decode=decode, eviction="lfu")
+        orc = OracleRun(w, st.info["slot_bytes"], policy="lfu")
+        lru = OracleRun(w, st.info["slot_bytes"])
+        ys, parted = [], False
+        for T in (1, 2):
+            xs = {l: st.hiddens(l, T, w.steps) for l in range(w.L)}
+            for step in range(w.steps):
+                for l in range(w.L):
+                    x = xs[l][step]
+                    ys.append(st.forward(x, l))
+                    ids, _ = orc.route(x, st.router[l], st.bias)
+                    plan = orc.plan(l, ids, T)
+                    compare_trace(st.cache.trace_read()[0], ids, plan, l, T)
+                    parted |= not np.array_equal(lru.plan(l, ids, T)["slot_of"], plan["slot_of"])
+                    if step % 6 == 0:
+                        _, _, yo = orc.layer(x, st.router[l], st.bias, l)
+                        assert rel_l2(ys[-1], yo) <= TOL
+        assert parted
+        runs[decode] = np.concatenate([y.reshape(-1) for y in ys])
+        st.close()
+    assert np.array_equal(runs["one_kernel"], runs["three_kernels"])
+
+
 def test_exact_ties_one_token_on_both_decode_paths():
     # One token per call: the one-kernel path ranks with one thread per
     # expert and certifies with a block-wide AND; exact ties fail the
