@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
     ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
                     help="decode launch mode (auto: one kernel for one- or two-token calls on per-layer pools)")
+    ap.add_argument("--eviction", default="lru", choices=["lru", "lfu"],
+                    help="slot eviction policy of the cache (least recently / least frequently used)")
     ap.add_argument("--prefill", action="store_true",
                     help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()
@@ -274,7 +276,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
-                          max_tokens=max(T, 1), device=local, decode=args.decode)
+                          max_tokens=max(T, 1), device=local, decode=args.decode, eviction=args.eviction)
     t_setup = time.perf_counter()
     cache = pec.MoECache(cfg)
     buf = None
@@ -497,7 +499,7 @@ def run_ours(args):
                    "inter": w.I, "format": w.fmt, "slots_per_layer": w.slots_per_layer,
                    "pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
                    "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
-                   "cache_priming_steps": PRIME,
+                   "cache_priming_steps": PRIME, "eviction": args.eviction,
                    "l2": "inputs larger than L2: each step reads ~1 GB of distinct expert bytes from an "
                          f"{info['pool_device_bytes'] / 1e9:.1f} GB slot pool"},
         "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
