@@ -147,15 +147,15 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same workload
 # ---------------------------------------------------------------------------
-def cpu_sample(w, T, budget_s, layers_per_step=None):
-    """Runs the oracle (routing, literal LRU, unpaged layer) token by token
+def cpu_sample(w, T, budget_s, layers_per_step=None, policy="lru"):
+    """Runs the oracle (routing, literal LRU or LFU, unpaged layer) token by token
     through the workload's layers until budget_s is spent; returns tok/s."""
     import numpy as np
     import oracle
     import synth
     cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer if w.pool_mode == "per_layer" else
                          oracle.slots_for_budget(w.pool_bytes, oracle.slot_bytes(w.fmt, w.H, w.I)),
-                         oracle.slot_bytes(w.fmt, w.H, w.I))
+                         oracle.slot_bytes(w.fmt, w.H, w.I), policy=policy)
     bias = synth.zipf_bias(w.E) if w.bias else None
     routers = {}
     recs = {}
@@ -208,7 +208,8 @@ def run_reference(args):
     import numpy as np
     import oracle
     import synth
-    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer, oracle.slot_bytes(w.fmt, w.H, w.I))
+    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer, oracle.slot_bytes(w.fmt, w.H, w.I),
+                         policy=args.eviction)
     bias = synth.zipf_bias(w.E) if w.bias else None
     total = args.warmup + args.steps
     routers, xs, recs = {}, {}, {}
@@ -239,7 +240,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k,
-                       "format": w.fmt, "slots_per_layer": w.slots_per_layer},
+                       "format": w.fmt, "slots_per_layer": w.slots_per_layer, "eviction": args.eviction},
             "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -486,7 +487,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
-        v, layers, secs = cpu_sample(w, T, args.cpu_seconds)
+        v, layers, secs = cpu_sample(w, T, args.cpu_seconds, policy=args.eviction)
         cpu = {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
                "sample": f"{layers} layer calls ({layers / w.L:.2f} tokens) of the same workload, "
                          f"{secs:.1f} s of fp64 oracle time on 1 host thread"}
