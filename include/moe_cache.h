@@ -286,9 +286,10 @@ moe_status_t moe_cache_profile_read(moe_cache_t* h, moe_profile_t* out);
 
 /* Router + top-k of one layer that allocates nothing (no counterpart on the
  * pages: it exists for callers of this library that cannot call cudaMalloc
- * where they route tokens -- code running inside CUDA graph capture, custom
- * allocators that must not be re-entered from their own callbacks, embedders
- * that budget all device memory up front). Computes, for T tokens, the same
+ * where they route tokens -- custom allocators that must not be re-entered
+ * from their own callbacks, embedders that budget all device memory up front,
+ * and latency-critical loops that cannot take cudaMalloc's implicit device
+ * synchronisation). Computes, for T tokens, the same
  * routing as moe_layer_forward: logits = hidden x router_w^T (+ bias), the
  * top_k experts with ties to the lower id, and their weights (softmax over the
  * picks when norm_topk, else the full softmax read at the picks).
@@ -298,7 +299,8 @@ moe_status_t moe_cache_profile_read(moe_cache_t* h, moe_profile_t* out);
  *   ids         : device int32 [T x top_k] (output, rank order per token)
  *   weights     : device fp32 [T x top_k] (output)
  * Limits: T <= 32, num_experts <= 512, top_k <= 16, hidden_size a multiple of
- * 64 up to 4096; anything else returns MOE_ERR_INVALID without launching.
+ * 64 up to 4096 (any such size: the router reads 256-column rounds and the last
+ * one may be partial); anything else returns MOE_ERR_INVALID without launching.
  * Scratch: a fixed 196,864-byte array inside the library, held by every GPU
  * that loads it until the process exits; no call allocates or frees memory.
  * The first call on a device looks up the array's device address (make that

@@ -155,9 +155,53 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _refuse(msg):
+    raise MoeError(ERR_INVALID, msg)
+
+
+def _check_noalloc_args(hidden, router_w, ids, weights, top_k, bias):
+    """Shapes, dtypes, devices and layouts of moe_route_topk_noalloc's tensors,
+    checked before the C call: the kernel writes ids[t * k + j] and weights[t *
+    k + j] for every token, so an undersized or mistyped output would be
+    written out of bounds on the device."""
+    import torch
+    for name, t in (("hidden", hidden), ("router_w", router_w), ("ids", ids), ("weights", weights)):
+        if not isinstance(t, torch.Tensor):
+            _refuse(f"{name} must be a torch tensor")
+    if hidden.dim() != 2 or router_w.dim() != 2:
+        _refuse("hidden must be [T, H] and router_w [E, H]")
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    if router_w.shape[1] != H:
+        _refuse(f"router_w has {router_w.shape[1]} columns, hidden has {H}")
+    if hidden.element_size() != 2 or router_w.element_size() != 2:
+        _refuse("hidden and router_w must hold 16-bit (bf16) values")
+    if not isinstance(top_k, int) or top_k < 1:
+        _refuse("top_k must be a positive int")
+    if tuple(ids.shape) != (T, top_k) or ids.dtype != torch.int32:
+        _refuse(f"ids must be int32 [{T}, {top_k}]")
+    if tuple(weights.shape) != (T, top_k) or weights.dtype != torch.float32:
+        _refuse(f"weights must be float32 [{T}, {top_k}]")
+    tensors = [hidden, router_w, ids, weights]
+    if bias is not None:
+        if not isinstance(bias, torch.Tensor) or tuple(bias.shape) != (E,) or bias.dtype != torch.float32:
+            _refuse(f"bias must be float32 [{E}]")
+        tensors.append(bias)
+    if not all(t.is_contiguous() for t in tensors):
+        _refuse("every tensor must be contiguous")
+    if not all(t.is_cuda for t in tensors):
+        _refuse("every tensor must be on a CUDA device")
+    dev = torch.cuda.current_device()
+    if any(t.device.index != dev for t in tensors):
+        _refuse(f"every tensor must be on the current CUDA device (cuda:{dev})")
+
+
 def route_topk_noalloc(hidden, router_w, ids, weights, top_k, bias=None, norm_topk=True, stream=None):
     """moe_route_topk_noalloc: routing of T tokens into caller-provided ids
-    [T, k] (int32) and weights [T, k] (fp32), with no allocation."""
+    [T, k] (int32) and weights [T, k] (fp32), with no allocation. The tensors
+    are checked (shape, dtype, device, contiguity) before the call; a mismatch
+    raises MoeError(ERR_INVALID) and launches nothing."""
+    _check_noalloc_args(hidden, router_w, ids, weights, top_k, bias)
     T, H = hidden.shape
     E = router_w.shape[0]
     if stream is None:

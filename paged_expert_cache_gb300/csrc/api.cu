@@ -295,6 +295,8 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.copy_slot, U);
     DA(s.act, P * d.I);
     DA(s.part, P * d.H);
+    DA(s.tok_shift, T);
+    DA(s.act_amax, P);
     DA(s.plan, 1);
     DA(s.route_done, 1);
     DA(s.tile_done, (size_t)d.H / 16);
@@ -320,7 +322,8 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         cudaMemset(s.copy_done, 0, 4) != cudaSuccess || cudaMemset(s.copy_t0, 0xff, 8) != cudaSuccess ||
         cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess ||
         cudaMemset(s.tiles_done, 0, 4) != cudaSuccess || cudaMemset(s.grid_bar, 0, 4) != cudaSuccess ||
-        cudaMemset(s.err, 0, 4) != cudaSuccess || cudaMemset(s.logit_ctr, 0, 8) != cudaSuccess)
+        cudaMemset(s.err, 0, 4) != cudaSuccess || cudaMemset(s.logit_ctr, 0, 8) != cudaSuccess ||
+        cudaMemset(s.tok_shift, 0, T * sizeof(int)) != cudaSuccess || cudaMemset(s.act_amax, 0, P * 4) != cudaSuccess)
         return bail(MOE_ERR_CUDA, "scratch initialisation failed");
     if (c.upload_mode == MOE_UPLOAD_MEMCPY) {
         e = cudaHostAlloc((void**)&h->host_fill, sizeof(int) * (2 + 2 * U), cudaHostAllocDefault);

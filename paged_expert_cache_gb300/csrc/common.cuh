@@ -100,6 +100,8 @@ struct Scratch {
     unsigned* logit_ctr;    // [2] logit CTAs done, per call parity (one-kernel decode)
     int2* gemm_items;       // prefill GEMM work list: (unit, 128-pair tile)
     int* gemm_count;        // its length
+    int* tok_shift;         // [T] power-of-two prescale of each token row (token_shift)
+    unsigned* act_amax;     // [P] largest |activation| of each pair, as fp32 bits (act_shift)
 };
 
 // Device cache state and constants of a handle.
@@ -214,6 +216,44 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+
+// ---------------------------------------------------------------------------
+// Power-of-two prescale of the fp16 tensor-core operands.
+//
+// fp16 holds normal values from 2^-14 to 65504 only, while bf16 tokens reach
+// about 3.4e38 and the fp32 SwiGLU activations anything fp32 holds. So each
+// token row, and each pair's activation row, is multiplied by 2^-s before it
+// is converted to fp16, with s chosen from the row's largest magnitude, and
+// the fp32 result of its MMAs is multiplied by 2^s afterwards. Both products
+// are exact (a power of two, away from fp32's overflow and subnormals), so the
+// scaling changes no result except where fp16 could not hold the row:
+//  - tokens: the row maximum lands at exponent 15, at most 65280 for a bf16
+//    value; bf16 values down to 2^-32 of the row maximum convert exactly;
+//  - activations (an fp16 hi + lo pair): the row maximum lands at exponent 14,
+//    so hi never rounds up past 65504.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int prescale_shift(unsigned maxbits_f32, int top) {
+    if (maxbits_f32 == 0u) return 0;
+    const int e = (int)((maxbits_f32 >> 23) & 0xffu) - 127;
+    const int s = e - top;
+    return s < -120 ? -120 : (s > 120 ? 120 : s);
+}
+// 2^s as a float, for |s| <= 126.
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
+// Shift of a token row from the largest |bf16| bit pattern of the row.
+__device__ __forceinline__ int token_shift(unsigned max_abs_bf16) { return prescale_shift((max_abs_bf16 & 0x7fffu) << 16, 15); }
+// Shift of an activation row from the bits of its largest |value|.
+__device__ __forceinline__ int act_shift(unsigned max_abs_f32) { return prescale_shift(max_abs_f32, 14); }
+// Largest |bf16| bit pattern (sign cleared) of the two halves of a word.
+__device__ __forceinline__ unsigned bf16x2_absmax(uint32_t w) {
+    const uint32_t m = w & 0x7fff7fffu;
+    return max(m & 0xffffu, m >> 16);
+}
+// The SwiGLU of one (row, pair) from the unscaled-by-2^-s sums: the one
+// expression every gate/up path uses, so their results agree bit for bit.
+__device__ __forceinline__ float swiglu_scaled(float gs, float us, float g0, float g1, float up) {
+    return silu_f(gs * g0 * up) * (us * g1 * up);
+}
 
 // Programmatic dependent launch: wait for the preceding grid's results, and
 // let the following grid be scheduled.

@@ -71,11 +71,13 @@ __global__ void __launch_bounds__(kGUWarps * 32, (FMT == FMT_Q4_0 || FMT == FMT_
                         const int t = pair_token(pair_at(s, d, n0 + nn), T, k);
                         val = *reinterpret_cast<const uint4*>(x + (size_t)t * H + v * 8);
                         if constexpr (FMT != FMT_BF16) {
+                            // fp16 with the token's power-of-two prescale (exact)
+                            const float sc = pow2f(-__ldg(s.tok_shift + t));
                             uint32_t w4[4] = {val.x, val.y, val.z, val.w};
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                const float lo = __uint_as_float(w4[j] << 16);
-                                const float hi = __uint_as_float(w4[j] & 0xffff0000u);
+                                const float lo = __uint_as_float(w4[j] << 16) * sc;
+                                const float hi = __uint_as_float(w4[j] & 0xffff0000u) * sc;
                                 w4[j] = h2_as_u32(__floats2half2_rn(lo, hi));
                             }
                             val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -116,10 +118,13 @@ __global__ void __launch_bounds__(kGUWarps * 32, (FMT == FMT_Q4_0 || FMT == FMT_
                 gs += red[(size_t)(w * 2) * 128 + threadIdx.x];
                 us += red[(size_t)(w * 2 + 1) * 128 + threadIdx.x];
             }
-            if (n0 + col < np) {
-                const int pair = pair_at(s, d, n0 + col);
-                s.act[(size_t)pair * I + rt * 16 + row] = silu_f(gs * d.g[0]) * (us * d.g[1]);
+            const int pair = n0 + col < np ? pair_at(s, d, n0 + col) : -1;
+            float a = 0.f;
+            if (pair >= 0) {
+                const float up = FMT == FMT_BF16 ? 1.0f : pow2f(__ldg(s.tok_shift + pair_token(pair, T, k)));
+                a = swiglu_scaled(gs, us, d.g[0], d.g[1], up);
             }
+            store_act<FMT>(s, pair, I, rt * 16 + row, a);
         }
         __syncthreads();
     }
@@ -170,7 +175,11 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
     const int np = d.np;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cpw = (KC + kDNWarps - 1) / kDNWarps;
+    __shared__ int psh[8];  // the prescale of each of the eight pairs' activations
     for (int n0 = 0; n0 < np; n0 += 8) {
+        if (threadIdx.x < 8)
+            psh[threadIdx.x] = n0 + (int)threadIdx.x < np ? pair_act_shift<FMT>(s, pair_at(s, d, n0 + threadIdx.x)) : 0;
+        __syncthreads();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c0 = 0; c0 < cpw; c0 += kMaxChunksInFlight) {
             Chunk<FMT> cd[kMaxChunksInFlight];
@@ -205,22 +214,11 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
                     } else if (n0 + nn < np) {
                         a4 = *reinterpret_cast<const float4*>(s.act + (size_t)pair_at(s, d, n0 + nn) * I + v * 4);
                     }
-                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    const float sc = pow2f(-psh[nn]);
+                    const float av[4] = {a4.x * sc, a4.y * sc, a4.z * sc, a4.w * sc};
                     uint16_t hv[4], lv[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if constexpr (FMT == FMT_BF16) {
-                            __nv_bfloat16 h = __float2bfloat16_rn(av[j]);
-                            __nv_bfloat16 l = __float2bfloat16_rn(av[j] - __bfloat162float(h));
-                            hv[j] = *reinterpret_cast<uint16_t*>(&h);
-                            lv[j] = *reinterpret_cast<uint16_t*>(&l);
-                        } else {
-                            __half h = __float2half_rn(av[j]);
-                            __half l = __float2half_rn(av[j] - __half2float(h));
-                            hv[j] = *reinterpret_cast<uint16_t*>(&h);
-                            lv[j] = *reinterpret_cast<uint16_t*>(&l);
-                        }
-                    }
+                    for (int j = 0; j < 4; ++j) split_hi_lo<FMT>(av[j], hv[j], lv[j]);
                     *reinterpret_cast<uint2*>(xh + (size_t)nn * ld + v * 4) =
                         make_uint2(hv[0] | ((uint32_t)hv[1] << 16), hv[2] | ((uint32_t)hv[3] << 16));
                     *reinterpret_cast<uint2*>(xl + (size_t)nn * ld + v * 4) =
@@ -253,7 +251,7 @@ __global__ void __launch_bounds__(kDNWarps * 32) k_down(CacheDev c, Scratch s, f
             for (int w = 0; w < kDNWarps; ++w) sum += red[(size_t)w * 128 + threadIdx.x];
             if (n0 + col < np) {
                 const int pair = pair_at(s, d, n0 + col);
-                s.part[(size_t)pair * H + rt * 16 + row] = sum * d.g[2];
+                s.part[(size_t)pair * H + rt * 16 + row] = sum * d.g[2] * pow2f(psh[col]);
             }
         }
         __syncthreads();
@@ -315,9 +313,10 @@ __global__ void __launch_bounds__(kDRWarps * 32, 1) k_down_rows(CacheDev c, Scra
         uint4* dst = reinterpret_cast<uint4*>(sd);
         for (int j = tid; j < nw; j += nthr) dst[j] = __ldcg(src + j);
     }
-    down_stage_act<FMT>(s, P, I, ah, al);
+    __shared__ int psh[kDecodeMaxTokens * (kMaxTopK + 1)];  // the pairs' activation prescales
+    down_stage_act<FMT>(s, P, I, ah, al, psh);
     __syncthreads();
-    down_rows_tile<FMT>(c, s, sd, n_units, T, blockIdx.x, ah, al, ps, s.wts, out);
+    down_rows_tile<FMT>(c, s, sd, n_units, T, blockIdx.x, ah, al, psh, ps, s.wts, out);
     if (tid == 0 && atomicAdd(s.tiles_done, 1u) == gridDim.x - 1) {
         // the last tile of the call books the time misses were streamed
         __threadfence();

@@ -207,6 +207,45 @@ __device__ __forceinline__ int pair_at(const Scratch& s, const UnitDesc& d, int 
 
 __device__ __forceinline__ int pair_token(int pair, int T, int k) { return pair < T * k ? pair / k : pair - T * k; }
 
+// Writes the activation a of (pair, row i) and folds |a| into the pair's
+// maximum for the down projection's prescale. The lanes of a warp hold four
+// rows of the eight columns lane & 7 (the gate/up epilogue layout); every lane
+// of the warp calls it, with pair < 0 where it holds no pair.
+template <int FMT>
+__device__ __forceinline__ void store_act(const Scratch& s, int pair, int I, int i, float a) {
+    if (pair >= 0) s.act[(size_t)pair * I + i] = a;
+    if constexpr (FMT != FMT_BF16) {
+        unsigned m = pair >= 0 ? __float_as_uint(fabsf(a)) : 0u;
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if ((threadIdx.x & 24) == 0 && pair >= 0) atomicMax(s.act_amax + pair, m);
+    }
+}
+
+// The prescale of a pair's activations (0 for bf16 experts, whose 16-bit
+// parts have fp32's range).
+template <int FMT>
+__device__ __forceinline__ int pair_act_shift(const Scratch& s, int pair) {
+    if constexpr (FMT == FMT_BF16) return 0;
+    else return act_shift(__ldcg(s.act_amax + pair));
+}
+
+// An fp32 value as two 16-bit parts, hi + lo (fp16, or bf16 for bf16 experts).
+template <int FMT>
+__device__ __forceinline__ void split_hi_lo(float v, uint16_t& hv, uint16_t& lv) {
+    if constexpr (FMT == FMT_BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+        hv = *reinterpret_cast<uint16_t*>(&h);
+        lv = *reinterpret_cast<uint16_t*>(&l);
+    } else {
+        __half h = __float2half_rn(v);
+        __half l = __float2half_rn(v - __half2float(h));
+        hv = *reinterpret_cast<uint16_t*>(&h);
+        lv = *reinterpret_cast<uint16_t*>(&l);
+    }
+}
+
 constexpr int kGUWarps = 8;
 constexpr int kDNWarps = 4;
 constexpr int kMaxChunksInFlight = 4;
@@ -245,11 +284,14 @@ __host__ __device__ inline size_t down_rows_smem(int I, int KC, int U, int P) {
 }
 
 // Stages the P activations of the call (fp32, written by the gate/up pass)
-// as hi + lo 16-bit parts, plus the zero row; every thread of the CTA takes
-// part, the caller synchronises.
+// as hi + lo 16-bit parts of the prescaled values, plus the zero row, and the
+// pairs' prescales in psh [P]; every thread of the CTA takes part, the caller
+// synchronises.
 template <int FMT>
-__device__ __forceinline__ void down_stage_act(const Scratch& s, int P, int I, uint16_t* ah, uint16_t* al) {
+__device__ __forceinline__ void down_stage_act(const Scratch& s, int P, int I, uint16_t* ah, uint16_t* al, int* psh) {
     const int ld = I + 8, tid = threadIdx.x, nthr = blockDim.x;
+    for (int p = tid; p < P; p += nthr) psh[p] = pair_act_shift<FMT>(s, p);
+    __syncthreads();
     const int vpr = I / 4;
     const int nv = P * vpr;
     constexpr int B = 4;
@@ -265,22 +307,11 @@ __device__ __forceinline__ void down_stage_act(const Scratch& s, int P, int I, u
             const int j = base + i * nthr;
             if (j < nv) {
                 const int pr = j / vpr, cv = j - pr * vpr;
-                const float av[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                const float sc = pow2f(-psh[pr]);
+                const float av[4] = {v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc};
                 uint16_t hv[4], lv[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if constexpr (FMT == FMT_BF16) {
-                        __nv_bfloat16 h = __float2bfloat16_rn(av[q]);
-                        __nv_bfloat16 l = __float2bfloat16_rn(av[q] - __bfloat162float(h));
-                        hv[q] = *reinterpret_cast<uint16_t*>(&h);
-                        lv[q] = *reinterpret_cast<uint16_t*>(&l);
-                    } else {
-                        __half h = __float2half_rn(av[q]);
-                        __half l = __float2half_rn(av[q] - __half2float(h));
-                        hv[q] = *reinterpret_cast<uint16_t*>(&h);
-                        lv[q] = *reinterpret_cast<uint16_t*>(&l);
-                    }
-                }
+                for (int q = 0; q < 4; ++q) split_hi_lo<FMT>(av[q], hv[q], lv[q]);
                 *reinterpret_cast<uint2*>(ah + (size_t)pr * ld + cv * 4) =
                     make_uint2(hv[0] | ((uint32_t)hv[1] << 16), hv[2] | ((uint32_t)hv[3] << 16));
                 *reinterpret_cast<uint2*>(al + (size_t)pr * ld + cv * 4) =
@@ -300,7 +331,7 @@ __device__ __forceinline__ void down_stage_act(const Scratch& s, int P, int I, u
 // weights wts. Run by kDRWarps warps; starts and ends with the CTA in step.
 template <int FMT>
 __device__ void down_rows_tile(const CacheDev& c, const Scratch& s, const UnitDesc* sd, int n_units, int T, int rt,
-                               const uint16_t* ah, const uint16_t* al, float* ps, const float* wts,
+                               const uint16_t* ah, const uint16_t* al, const int* psh, float* ps, const float* wts,
                                float* __restrict__ out) {
     constexpr int IB = FMT == FMT_BF16 ? 1 : 2;  // items a warp keeps in flight
     const int H = c.H, I = c.I, KC = I / 64, k = c.k;
@@ -368,7 +399,7 @@ __device__ void down_rows_tile(const CacheDev& c, const Scratch& s, const UnitDe
                         const int cc = 2 * q + c2;
                         if (n0 + cc < d.np) {
                             const int pair = n0 + cc < 8 ? d.pair8[n0 + cc] : s.unit_pairs[d.pstart + n0 + cc];
-                            ps[((size_t)cg * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
+                            ps[((size_t)cg * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd * pow2f(psh[pair]);
                         }
                     }
                 }

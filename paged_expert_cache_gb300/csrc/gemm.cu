@@ -27,9 +27,12 @@
 // in fp16 (an E2M1 value times an E4M3 scale has at most five significant
 // bits), and the per-matrix global scale is applied in the epilogue. Q4_0 and
 // block-FP8 weights are rounded once to fp16 (relative error <= 2^-11). Tokens
-// (bf16) are exact in fp16. The down projection takes each fp32 activation as
-// an fp16 hi + lo pair, two MMAs into one accumulator, as the decode kernels
-// do. bf16 experts keep the mma.sync kernels (their operands would be bf16).
+// (bf16) enter as fp16 after the power-of-two prescale of their row (common.cuh),
+// which keeps every value within 2^-32 of the row's largest exact, whatever
+// the row's magnitude. The down projection takes each prescaled fp32
+// activation as an fp16 hi + lo pair, two MMAs into one accumulator, as the
+// decode kernels do. bf16 experts keep the mma.sync kernels (their operands
+// would be bf16).
 #include "expert_dev.cuh"
 
 namespace moe {
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
     __shared__ uint32_t tmem_base;
     __shared__ int tok[kGN];
     __shared__ int pairs[kGN];
+    __shared__ int tsh[kGN];  // each column's token prescale (token_shift)
     griddep_wait();
     if ((int)blockIdx.x >= *count) return;
     const int2 it = items[blockIdx.x];
@@ -274,6 +278,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
         const int p = tid < nn ? s.unit_pairs[d.pstart + n0 + tid] : -1;
         pairs[tid] = p;
         tok[tid] = p >= 0 ? pair_token(p, T, k) : -1;
+        tsh[tid] = p >= 0 ? __ldg(s.tok_shift + tok[tid]) : 0;
     }
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tc_fence_before();
@@ -317,14 +322,16 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
             frag_to_f16<FMT>(cu, a);
             store_frag(stage + kGTile, warp, lane, a);
         }
-        // tokens: bf16 -> fp16 (bf16 values are exact in fp16)
+        // tokens: bf16 -> fp16 with the token's power-of-two prescale (exact)
 #pragma unroll
         for (int r = 0; r < kTokPerThread; ++r) {
             const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
+            const float sc = pow2f(-tsh[j]);
             uint32_t w4[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                w4[q] = h2_as_u32(__floats2half2_rn(__uint_as_float(w4[q] << 16), __uint_as_float(w4[q] & 0xffff0000u)));
+                w4[q] = h2_as_u32(__floats2half2_rn(__uint_as_float(w4[q] << 16) * sc,
+                                                    __uint_as_float(w4[q] & 0xffff0000u) * sc));
             *reinterpret_cast<uint4*>(stage + 2 * kGTile + sw128(j, cc * 8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         if (kc + 1 < KC) load_next(kc + 1);
@@ -363,13 +370,32 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
             tc_ld32(tmem + ((uint32_t)(32 * lq) << 16) + col, g);
             tc_ld32(tmem + ((uint32_t)(32 * lq) << 16) + kGN + col, u);
             tc_ld_wait();
+            unsigned mx[32];  // |a| bits of this lane's row, per column
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int p = pairs[col + j];
-                if (p >= 0)
-                    s.act[(size_t)p * I + i_out] =
-                        silu_f(__uint_as_float(g[j]) * d.g[0]) * (__uint_as_float(u[j]) * d.g[1]);
+                mx[j] = 0u;
+                if (p >= 0) {
+                    const float av = swiglu_scaled(__uint_as_float(g[j]), __uint_as_float(u[j]), d.g[0], d.g[1],
+                                                   pow2f(tsh[col + j]));
+                    s.act[(size_t)p * I + i_out] = av;
+                    mx[j] = __float_as_uint(fabsf(av));
+                }
             }
+            // the largest |a| of each column over the warp's 32 rows, for the
+            // down projection's prescale: a transposing butterfly halves the
+            // columns a lane keeps at each step and leaves column `lane` in mx[0]
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int cc = 0; cc < off; ++cc) {
+                    const unsigned send = upper ? mx[cc] : mx[cc + off];
+                    const unsigned keep = upper ? mx[cc + off] : mx[cc];
+                    mx[cc] = max(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                }
+            }
+            if (pairs[col + lane] >= 0 && mx[0]) atomicMax(s.act_amax + pairs[col + lane], mx[0]);
         }
     }
     if (!ok && tid == 0) atomicOr(s.err, 4u);
@@ -391,6 +417,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
     __shared__ __align__(8) unsigned long long bars[kGStages];
     __shared__ uint32_t tmem_base;
     __shared__ int pairs[kGN];
+    __shared__ int psh[kGN];  // each column's activation prescale (act_shift)
     griddep_wait();
     if ((int)blockIdx.x >= *count) return;
     const int2 it = items[blockIdx.x];
@@ -407,7 +434,11 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
         tc_relinquish();
     }
     if (tid < kGStages) gbar_init(gsmem(&bars[tid]));
-    if (tid < kGN) pairs[tid] = tid < nn ? s.unit_pairs[d.pstart + n0 + tid] : -1;
+    if (tid < kGN) {
+        const int p = tid < nn ? s.unit_pairs[d.pstart + n0 + tid] : -1;
+        pairs[tid] = p;
+        psh[tid] = p >= 0 ? act_shift(__ldcg(s.act_amax + p)) : 0;
+    }
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
@@ -452,16 +483,18 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
             const int i = tid + r * kGThreads, j = i >> 3, cc = i & 7;
             uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
             {
+                const float sc = pow2f(-psh[j]);  // the pair's prescale (exact)
                 const float4 f0 = av[r][0], f1 = av[r][1];
-                const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                const float f[8] = {f0.x * sc, f0.y * sc, f0.z * sc, f0.w * sc,
+                                    f1.x * sc, f1.y * sc, f1.z * sc, f1.w * sc};
+                uint16_t h16[8], l16[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) split_hi_lo<FMT>(f[q], h16[q], l16[q]);
                 uint32_t h[4], l[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const __half a0 = __float2half_rn(f[2 * q]), a1 = __float2half_rn(f[2 * q + 1]);
-                    const __half b0 = __float2half_rn(f[2 * q] - __half2float(a0));
-                    const __half b1 = __float2half_rn(f[2 * q + 1] - __half2float(a1));
-                    h[q] = h2_as_u32(__halves2half2(a0, a1));
-                    l[q] = h2_as_u32(__halves2half2(b0, b1));
+                    h[q] = (uint32_t)h16[2 * q] | ((uint32_t)h16[2 * q + 1] << 16);
+                    l[q] = (uint32_t)l16[2 * q] | ((uint32_t)l16[2 * q + 1] << 16);
                 }
                 hv = make_uint4(h[0], h[1], h[2], h[3]);
                 lv = make_uint4(l[0], l[1], l[2], l[3]);
@@ -502,7 +535,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int p = pairs[col + j];
-                if (p >= 0) s.part[(size_t)p * H + h_out] = __uint_as_float(v[j]) * d.g[2];
+                if (p >= 0) s.part[(size_t)p * H + h_out] = __uint_as_float(v[j]) * d.g[2] * pow2f(psh[col + j]);
             }
         }
     }

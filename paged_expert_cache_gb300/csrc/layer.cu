@@ -534,6 +534,8 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     __shared__ unsigned long long clk;
     __shared__ int rerank;
     __shared__ int slot_err;
+    __shared__ unsigned tmax[kLayerMaxTokens];  // largest |bf16| bits of each token (its fp16 prescale)
+    __shared__ int psh[kLayerMaxPairs];         // the pairs' activation prescales
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
     const int E = c.E, H = c.H, I = c.I, k = c.k, T = kOneToken ? 1 : a.T;
@@ -576,7 +578,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     const int e_mine = warp < kLogitWarps ? b * kLogitWarps + warp : E;
     uint16_t* wr = reinterpret_cast<uint16_t*>(smem + L.wr) + (size_t)warp * H;
     if (e_mine < E)
-        for (int i = 0; i < H / 256; ++i)
+        for (int i = 0; i < router_nvec(H) && lane * 8 + i * 256 < H; ++i)
             cp_async16(wr + lane * 8 + i * 256, a.w + (size_t)e_mine * H + lane * 8 + i * 256);
     const PlanSmem m = plan_layout(smem + L.plan, E, c.K, n_ids, U, P);
     // the pool's state (stamps, keys, the layer's slot map, its clock, NVFP4
@@ -607,6 +609,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
         // the tokens, and the pool's state if not staged yet
         for (int i = tid; i < T * (H / 8); i += kLThreads) cp_async16(xs + (size_t)i * 8, a.x + (size_t)i * 8);
         if (!a.early) stage_state();
+        if (tid < kLayerMaxTokens) tmax[tid] = 0u;
+        // the pairs' activation maxima start from zero; this is ordered before
+        // every other CTA's gate/up by the logit announcement (or the grid
+        // barrier) below, and after the previous call's readers by the wait
+        if (b == 0)
+            for (int i = tid; i < P; i += kLThreads) s.act_amax[i] = 0u;
         for (int i = tid; i < E; i += kLThreads) m.first[i] = 0x7fffffff;
         for (int i = tid; i <= E / 32; i += kLThreads) m.missbits[i] = 0u;
         if (tid == 0) {
@@ -629,16 +637,32 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     }
     {
         // f16 copy of the tokens for the expert B operand (converted as the
-        // gate/up kernel does); row T is zero
+        // gate/up kernel does, with each token's power-of-two prescale, taken
+        // from the token's largest magnitude as the routing kernel takes it);
+        // row T is zero
+        if constexpr (FMT != FMT_BF16) {
+            for (int t = 0; t < T; ++t) {
+                unsigned mx = 0u;
+                for (int v = tid; v < H / 8; v += kLThreads) {
+                    const uint4 val = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + v * 8);
+                    mx = max(mx, max(max(bf16x2_absmax(val.x), bf16x2_absmax(val.y)),
+                                     max(bf16x2_absmax(val.z), bf16x2_absmax(val.w))));
+                }
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                if (lane == 0 && mx) atomicMax(&tmax[t], mx);
+            }
+            __syncthreads();
+        }
         for (int i = tid; i < T * (H / 8); i += kLThreads) {
             const int t = i / (H / 8), v = i - t * (H / 8);
             const uint4 val = *reinterpret_cast<const uint4*>(xs + (size_t)i * 8);
             uint32_t w4[4] = {val.x, val.y, val.z, val.w};
             if constexpr (FMT != FMT_BF16) {
+                const float sc = pow2f(-token_shift(tmax[t]));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float lo = __uint_as_float(w4[j] << 16);
-                    const float hi = __uint_as_float(w4[j] & 0xffff0000u);
+                    const float lo = __uint_as_float(w4[j] << 16) * sc;
+                    const float hi = __uint_as_float(w4[j] & 0xffff0000u) * sc;
                     w4[j] = h2_as_u32(__floats2half2_rn(lo, hi));
                 }
             }
@@ -836,10 +860,13 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
                     gs += red[(size_t)(w * 2) * 128 + gtid];
                     us += red[(size_t)(w * 2 + 1) * 128 + gtid];
                 }
-                if (cc < np) {
-                    const int pair = pair_at(s, d, cc);
-                    s.act[(size_t)pair * I + rt * 16 + row] = silu_f(gs * d.g[0]) * (us * d.g[1]);
+                const int pair = cc < np ? pair_at(s, d, cc) : -1;
+                float av = 0.f;
+                if (pair >= 0) {
+                    const float up = FMT == FMT_BF16 ? 1.0f : pow2f(token_shift(tmax[pair_token(pair, T, k)]));
+                    av = swiglu_scaled(gs, us, d.g[0], d.g[1], up);
                 }
+                store_act<FMT>(s, pair, I, rt * 16 + row, av);
             }
             if (Dg && gtid == 0) atomicMax(s.copy_t1, globaltimer_ns());
             group_sync(grp);
@@ -881,7 +908,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
         const int ld = I + 8;
         const int ncg = (KCD + kDRChunks - 1) / kDRChunks;
         const uint32_t len0 = (uint32_t)KCD * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
-        down_stage_act<FMT>(s, P, I, ah, al);
+        down_stage_act<FMT>(s, P, I, ah, al, psh);
         __syncthreads();
         const int g = lane >> 2, qd = lane & 3;
         for (int r = 0; r < q.n_rt; ++r) {
@@ -922,7 +949,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
                         const int cc = 2 * qd + c2;
                         if (cc < d.np) {
                             const int pair = d.pair8[cc];
-                            ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd;
+                            ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd * pow2f(psh[pair]);
                         }
                     }
                 }

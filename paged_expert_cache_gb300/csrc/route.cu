@@ -19,7 +19,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(const __grid_constan
     extern __shared__ __align__(16) uint8_t smem[];
     griddep_wait();
     griddep_launch();
-    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds);
+    {
+        // the pairs' activation maxima start from zero for the expert kernels
+        // that follow (the previous call's readers have completed)
+        const int P = a.T * c.k + (c.has_shared ? a.T : 0);
+        const int nthr = blockDim.x * gridDim.x * gridDim.y;
+        for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < P; i += nthr)
+            s.act_amax[i] = 0u;
+    }
+    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds, s.tok_shift);
     if (a.prefill) return;
     __threadfence();
     __syncthreads();
@@ -253,10 +261,10 @@ void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a
 // ---------------------------------------------------------------------------
 // Router + top-k for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc where they route tokens: code running
-// while a CUDA graph is being captured (an allocation there breaks the
-// capture), allocators that must not be re-entered from their own callbacks,
-// and embedders that budget every byte of device memory up front. For them
+// Some callers cannot call cudaMalloc where they route tokens: allocators that
+// must not be re-entered from their own callbacks, embedders that budget every
+// byte of device memory up front, and latency-critical loops that cannot take
+// cudaMalloc's implicit device synchronisation. For them
 // moe_route_topk_noalloc computes one layer's routing (logits, top-k,
 // weights) without allocating: its scratch (the logit pairs, their bounds
 // and a completion counter) lives in the file-scope array below, which every
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route_noalloc(const __grid
                                                                  const __grid_constant__ Scratch s,
                                                                  const __grid_constant__ RouteArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds);
+    router_logits_tile<NT>(c, a, smem, s.logits, s.bounds, nullptr);
     __threadfence();
     __syncthreads();
     __shared__ int is_last;

@@ -87,14 +87,25 @@ __device__ __forceinline__ bool pair_eq(float2 a, float2 b) { return a.x == b.x 
 
 constexpr int kRouterMaxVec = 16;  // H <= 4096: a lane's router vectors, all in flight at once
 
-// The lane's share of router row e: 16-byte vectors lane*8 + i*256.
+// Router vectors per lane: lane l reads columns l*8 + i*256 .. +7 for
+// i < router_nvec(H) while they lie below H (H is a multiple of 64, so the
+// last round is partial when H is not a multiple of 256: lanes past the row's
+// end skip it).
+__host__ __device__ __forceinline__ int router_nvec(int H) { return (H + 255) / 256; }
+
+// The lane's share of router row e: 16-byte vectors lane*8 + i*256 < H.
 __device__ __forceinline__ void router_row_load(const uint16_t* w, int e, int H, int lane, uint4 (&wv)[kRouterMaxVec]) {
     const uint16_t* wr = w + (size_t)e * H;
-    const int nvec = H / 256;
+    const int nvec = router_nvec(H);
 #pragma unroll
     for (int i = 0; i < kRouterMaxVec; ++i)
-        if (i < nvec) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + lane * 8 + i * 256));
+        if (i < nvec && lane * 8 + i * 256 < H) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + lane * 8 + i * 256));
 }
+
+// The longest chain of roundings a lane's logit sum goes through: its eight
+// products per vector, then the five butterfly levels and the bias (with
+// room to spare); the error bounds below take it as n.
+__device__ __forceinline__ float router_chain(int H) { return (float)(8 * router_nvec(H) + 16); }
 
 // Logits of expert e for tokens t0 .. t0+nt-1 (staged bf16 in xs, [NT][H]),
 // one warp, with their bounds. Each lane sums its own columns in order with
@@ -107,11 +118,12 @@ static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a,
     float hi[NT], lo[NT], ab[NT];
 #pragma unroll
     for (int tt = 0; tt < NT; ++tt) hi[tt] = lo[tt] = ab[tt] = 0.f;
-    const int nvec = H / 256;
+    const int nvec = router_nvec(H);
 #pragma unroll
     for (int i = 0; i < kRouterMaxVec; ++i) {
         if (i >= nvec) break;
         const int cb = lane * 8 + i * 256;
+        if (cb >= H) continue;  // the partial last round
         float wf[8] = {bf16_lo(wv[i].x), bf16_hi(wv[i].x), bf16_lo(wv[i].y), bf16_hi(wv[i].y),
                        bf16_lo(wv[i].z), bf16_hi(wv[i].z), bf16_lo(wv[i].w), bf16_hi(wv[i].w)};
 #pragma unroll
@@ -154,7 +166,7 @@ static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a,
         // H * 2^-52 * S of it plus its own bias rounding (2^-52 |z|); folding
         // the bias into the pair costs at most 2^-46 |z|. Doubled, then
         // rounded up.
-        const float n = (float)(H / 32 + 16);
+        const float n = router_chain(H);
         const float g = n * 0x1p-24f / (1.0f - n * 0x1p-24f);
         float hv = hi[0], lv = lo[0], av = ab[0];
 #pragma unroll
@@ -184,10 +196,11 @@ static __device__ void router_logit_row(const CacheDev& c, const RouteArgs& a, c
                                         int t, int e, float2* logits, float* bounds) {
     const int H = c.H, E = c.E, lane = threadIdx.x & 31;
     float hi = 0.f, lo = 0.f, ab = 0.f;
-    const int nvec = H / 256;
+    const int nvec = router_nvec(H);
 #pragma unroll 1
     for (int i = 0; i < nvec; ++i) {
         const int cb = lane * 8 + i * 256;
+        if (cb >= H) break;  // the partial last round
         const uint4 wq = *reinterpret_cast<const uint4*>(row + cb);
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + cb);
         const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
@@ -217,7 +230,7 @@ static __device__ void router_logit_row(const CacheDev& c, const RouteArgs& a, c
     }
     if (lane == 0) {
         // the bound of router_logits_warp
-        const float n = (float)(H / 32 + 16);
+        const float n = router_chain(H);
         const float g = n * 0x1p-24f / (1.0f - n * 0x1p-24f);
         float2 z = norm_pair(hi, lo);
         if (a.bias) {
@@ -233,10 +246,21 @@ static __device__ void router_logit_row(const CacheDev& c, const RouteArgs& a, c
     }
 }
 
+// Largest |bf16| bit pattern of a token row of H values staged in shared
+// memory, by one warp (every lane returns it).
+__device__ __forceinline__ unsigned token_absmax_warp(const uint16_t* row, int H, int lane) {
+    unsigned m = 0u;
+    const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row);
+    for (int i = lane; i < H / 2; i += 32) m = max(m, bf16x2_absmax(r32[i]));
+    return __reduce_max_sync(0xffffffffu, m);
+}
+
 // Logits of one CTA's experts for one CTA's NT tokens, with their bounds.
+// tok_shift (or null): the CTAs of the first expert column write the
+// fp16 prescale of their tokens there (token_shift), for the expert kernels.
 template <int NT>
 static __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a, uint8_t* smem, float2* logits,
-                                   float* bounds) {
+                                   float* bounds, int* tok_shift) {
     const int H = c.H, E = c.E;
     const int t0 = blockIdx.y * NT;
     const int nt = min(NT, a.T - t0);
@@ -252,6 +276,11 @@ static __device__ void router_logits_tile(const CacheDev& c, const RouteArgs& a,
             reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + tt) * H)[cv];
     }
     __syncthreads();
+    if (tok_shift && blockIdx.x == 0)
+        for (int tt = warp; tt < nt; tt += kRouteWarps) {
+            const unsigned m = token_absmax_warp(xs + (size_t)tt * H, H, lane);
+            if (lane == 0) tok_shift[t0 + tt] = token_shift(m);
+        }
     if (e >= E) return;
     router_logits_warp<NT>(c, a, xs, t0, nt, e, wv, logits, bounds);
 }

@@ -32,7 +32,7 @@ class Setup:
     """A GPU cache plus the workload's device inputs."""
 
     def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
-                 multi_wave=False, eviction="lru"):
+                 multi_wave=False, eviction="lru", norm_topk=True):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -41,7 +41,7 @@ class Setup:
                               slots_per_layer=(K if K is not None else w.slots_per_layer),
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
-                              decode=decode, multi_wave=multi_wave, eviction=eviction)
+                              decode=decode, multi_wave=multi_wave, eviction=eviction, norm_topk=norm_topk)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):
@@ -80,8 +80,9 @@ class Setup:
 class OracleRun:
     """The same calls through the oracle: routing, literal LRU, unpaged layer."""
 
-    def __init__(self, w, slot_bytes, K=None, policy="lru"):
+    def __init__(self, w, slot_bytes, K=None, policy="lru", norm=True):
         self.w = w
+        self.norm = norm
         self.K = pool_slots(w, slot_bytes, K)
         self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy)
         self._rec = {}
@@ -94,7 +95,7 @@ class OracleRun:
 
     def route(self, x_bits, router, bias):
         z = oracle.router_logits(x_bits, router, bias)
-        return oracle.topk(z, self.w.k)
+        return oracle.topk(z, self.w.k, norm=self.norm)
 
     def plan(self, layer, ids, T):
         return self.cache.plan(layer, ids.reshape(-1), T)
@@ -105,7 +106,8 @@ class OracleRun:
         ids, _ = oracle.topk(z, w.k)
         recs = {int(e): self.record(layer, int(e)) for e in np.unique(ids)}
         shared = self.record(layer, -1) if w.has_shared else None
-        return oracle.moe_layer(w.fmt, w.H, w.I, w.E, w.k, recs, x_bits, router, bias, shared=shared)
+        return oracle.moe_layer(w.fmt, w.H, w.I, w.E, w.k, recs, x_bits, router, bias, shared=shared,
+                                norm=self.norm)
 
 
 def compare_trace(rec, ids, plan, layer, T):
@@ -117,3 +119,20 @@ def compare_trace(rec, ids, plan, layer, T):
     assert np.array_equal(rec["fill_expert"], plan["fill_expert"])
     assert np.array_equal(rec["fill_slot"], plan["fill_slot"])
     assert rec["n_hit"] == plan["n_hit"] and rec["n_uniq"] == plan["n_uniq"]
+
+
+def scale_bf16_rows(x_bits, factors):
+    """bf16 bit patterns [T, H] with row t multiplied by factors[t] (or by an
+    array broadcast against the row), rounded to nearest even: token rows of a
+    chosen magnitude, built on the test side as inputs."""
+    x = (np.asarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    f = np.asarray(factors, dtype=np.float64)
+    y = (x * (f[:, None] if f.ndim == 1 else f)).astype(np.float32)
+    u = y.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def rel_l2_rows(got, want):
+    """Relative L2 error of each row (token) separately."""
+    return [rel_l2(g, w) for g, w in zip(np.asarray(got), np.asarray(want))]

@@ -55,3 +55,31 @@ def test_multi_wave_flag_must_be_0_or_1():
     with pytest.raises(pec.MoeError) as ei:
         pec.MoECache(cfg)
     assert ei.value.status == pec.ERR_INVALID
+
+
+def test_noalloc_wrapper_refuses_mismatched_tensors_before_any_launch():
+    # The routing entry point writes ids[t * k + j] and weights[t * k + j] for
+    # every token: the binding refuses outputs of the wrong shape or dtype,
+    # inputs whose widths differ, and non-contiguous tensors before it calls
+    # the library (these CPU tensors never reach a kernel).
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((4, 256), dtype=torch.int16)
+    wr = torch.zeros((16, 256), dtype=torch.int16)
+    ids = torch.zeros((4, 2), dtype=torch.int32)
+    wts = torch.zeros((4, 2), dtype=torch.float32)
+    bad = [
+        (x, wr, torch.zeros((3, 2), dtype=torch.int32), wts, None, "ids"),
+        (x, wr, torch.zeros((4, 2), dtype=torch.int64), wts, None, "ids"),
+        (x, wr, ids, torch.zeros((4, 1), dtype=torch.float32), None, "weights"),
+        (x, wr, ids, torch.zeros((4, 2), dtype=torch.float64), None, "weights"),
+        (x, torch.zeros((16, 192), dtype=torch.int16), ids, wts, None, "columns"),
+        (x.float(), wr, ids, wts, None, "16-bit"),
+        (x, wr, ids, wts, torch.zeros(15, dtype=torch.float32), "bias"),
+        (x, wr, torch.zeros((2, 4), dtype=torch.int32).t(), wts, None, "contiguous"),
+        (x, wr, ids, wts, None, "CUDA device"),
+    ]
+    for h, r, i, w, b, what in bad:
+        with pytest.raises(pec.MoeError) as ei:
+            pec.route_topk_noalloc(h, r, i, w, 2, bias=b)
+        assert ei.value.status == pec.ERR_INVALID
+        assert what in str(ei.value), (what, str(ei.value))

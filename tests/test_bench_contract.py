@@ -28,7 +28,11 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys():
         assert key in d, key
     assert d["impl"] == "reference" and d["unit"] == "tok/s" and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
-    assert d["config"]["workload"] == "qwen3_30b_a3b_q4_0"
+    assert d["config"]["workload"] == "flash_next_nvfp4"
+    for key in ("batch", "layers", "experts", "top_k", "hidden", "inter", "format", "shared_expert", "pool",
+                "slots_per_pool", "pool_bytes", "eviction"):
+        assert key in d["config"], key
+    assert d["config"]["slots_per_pool"] == 4031 and d["config"]["shared_expert"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

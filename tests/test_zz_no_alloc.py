@@ -1,10 +1,11 @@
 """The routing entry point that allocates nothing (moe_route_topk_noalloc).
 
 It serves callers that cannot allocate device memory where they route
-tokens (for example code running under CUDA graph capture). Its ids must be
-exactly those moe_layer_forward routes the same tokens to, and its weights
-those of the oracle, on two calls in a row that share the library's fixed
-scratch array. Collected last so a failure here does not hide the others.
+tokens (allocators that must not be re-entered from their own callbacks,
+embedders that budget all device memory up front). Its ids must be exactly
+those moe_layer_forward routes the same tokens to, and its weights those of
+the oracle, on two calls in a row that share the library's fixed scratch
+array. Collected last so a failure here does not hide the others.
 """
 import numpy as np
 import pytest
@@ -15,16 +16,18 @@ from synth.workloads import WORKLOADS, scaled
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
 
 
-@pytest.mark.parametrize("name,T", [("qwen3_30b_a3b_fp8", 4), ("flash_next_nvfp4", 1), ("tiny", 4)])
-def test_noalloc_routing_matches_the_layer_forward(name, T):
+@pytest.mark.parametrize("name,T,H,norm", [("qwen3_30b_a3b_fp8", 4, 512, True), ("flash_next_nvfp4", 1, 512, True),
+                                            ("tiny", 4, 256, True), ("qwen3_30b_a3b_q4_0", 3, 320, True),
+                                            ("flash_next_nvfp4", 2, 512, False)])
+def test_noalloc_routing_matches_the_layer_forward(name, T, H, norm):
     import torch
     import paged_expert_cache_gb300 as pec
     base = WORKLOADS[name]
-    w = scaled(base, L=1, H=min(base.H, 512), I=128, streams=(T,), steps=2,
+    w = scaled(base, L=1, H=H, I=128, streams=(T,), steps=2,
                slots_per_layer=max(base.slots_per_layer, T * base.k), pool_bytes=0.0, pool_mode="per_layer",
                has_shared=False)
-    st = Setup(w, max_tokens=T)
-    orc = OracleRun(w, st.info["slot_bytes"])
+    st = Setup(w, max_tokens=T, norm_topk=norm)
+    orc = OracleRun(w, st.info["slot_bytes"], norm=norm)
     xs = st.hiddens(0, T, 2)
     ids = torch.empty((T, w.k), dtype=torch.int32, device=st.dev)
     wts = torch.empty((T, w.k), dtype=torch.float32, device=st.dev)
@@ -32,7 +35,7 @@ def test_noalloc_routing_matches_the_layer_forward(name, T):
         st.forward(xs[step], 0)
         rec = st.cache.trace_read()[0]
         x = torch.from_numpy(np.ascontiguousarray(xs[step]).view(np.int16)).to(st.dev)
-        pec.route_topk_noalloc(x, st.router_dev[0], ids, wts, w.k, bias=st.bias_dev)
+        pec.route_topk_noalloc(x, st.router_dev[0], ids, wts, w.k, bias=st.bias_dev, norm_topk=norm)
         torch.cuda.synchronize()
         got_ids = ids.cpu().numpy().reshape(-1)
         assert np.array_equal(got_ids, rec["ids"]), (got_ids, rec["ids"])
