@@ -1,13 +1,16 @@
 #!/usr/bin/env python3
 """Decode benchmark of the routed MoE FFN over the LRU expert cache.
 
-Workload (default): Qwen3-30B-A3B-shaped decode -- 48 MoE layers, 128 experts
-per layer, top-8, hidden 2048, expert intermediate 768, Q4_0 experts, 92 LRU
-slots per layer, batch 1, AR(1) hiddens (rho 0.9). One step is one decode
-token through all 48 layers: router + top-k, the cache plan, miss uploads
-from the pinned host store, gate/up + SwiGLU and down + combine, all through
-moe_layer_forward. Inputs are seeded synthetic stand-ins for the pages'
-checkpoints and prompts.
+Workload (default): Flash-Next-shaped decode -- 48 MoE layers, 512 routed
+experts per layer, top-10 plus one always-on shared expert, hidden 2048,
+expert intermediate 768, NVFP4 experts, one LRU pool of 10.7e9 bytes (4031
+slots) shared by all layers, batch 1, AR(1) hiddens (rho 0.9). It is the
+largest configuration that fits one GPU. --workload qwen3_30b_a3b_q4_0 (and
+the others of synth/workloads.py) time the other configurations. One step is
+one decode token through all 48 layers: router + top-k, the cache plan, miss
+uploads from the pinned host store, gate/up + SwiGLU and down + combine, all
+through moe_layer_forward. Inputs are seeded synthetic stand-ins for the
+pages' checkpoints and prompts.
 
 Prints ONE JSON line (rank 0). --impl reference times the CPU oracle instead.
 """
@@ -33,11 +36,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen3_30b_a3b_q4_0")
+    ap.add_argument("--workload", default="flash_next_nvfp4")
     ap.add_argument("--batch", type=int, default=0, help="tokens per call (default: the workload's first)")
     ap.add_argument("--profile-steps", type=int, default=32)
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU sample")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of each oracle CPU sample")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
     ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
@@ -76,6 +79,24 @@ def aggregate(ms, tokens, dist=None, device="cpu"):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
     return float(t.item()), int(n.item())
+
+
+def pool_slots(w):
+    """Slots of one pool: the per-layer K, or the shared budget over the slot size."""
+    if w.pool_mode == "per_layer":
+        return w.slots_per_layer
+    import oracle
+    return oracle.slots_for_budget(w.pool_bytes, oracle.slot_bytes(w.fmt, w.H, w.I))
+
+
+def bench_config(w, T, eviction):
+    """The workload a line measures; the same dict on both arms."""
+    return {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
+            "inter": w.I, "format": w.fmt, "shared_expert": w.has_shared, "pool": w.pool_mode,
+            "slots_per_pool": pool_slots(w), "pool_bytes": w.pool_bytes if w.pool_mode == "shared" else None,
+            "eviction": eviction, "router_bias": w.bias,
+            "l2": "inputs larger than L2: each decode step reads the records of ~0.5 k distinct experts "
+                  "(~1.3 GB at batch 1) from a slot pool of several GB"}
 
 
 def load_peaks():
@@ -147,25 +168,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same workload
 # ---------------------------------------------------------------------------
-def cpu_sample(w, T, budget_s, layers_per_step=None, policy="lru"):
+def cpu_sample(w, T, budget_s, layers_per_step=None, policy="lru", layer_set=None):
     """Runs the oracle (routing, literal LRU or LFU, unpaged layer) token by token
-    through the workload's layers until budget_s is spent; returns tok/s."""
+    through the workload's layers (or those of layer_set) until budget_s is
+    spent; returns (tok/s, layer calls, oracle seconds)."""
     import numpy as np
     import oracle
     import synth
-    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer if w.pool_mode == "per_layer" else
-                         oracle.slots_for_budget(w.pool_bytes, oracle.slot_bytes(w.fmt, w.H, w.I)),
-                         oracle.slot_bytes(w.fmt, w.H, w.I), policy=policy)
+    cache = oracle.Cache(w.L, w.E, w.pool_mode, pool_slots(w), oracle.slot_bytes(w.fmt, w.H, w.I), policy=policy)
+    layer_list = list(range(w.L if layers_per_step is None else layers_per_step)) if layer_set is None \
+        else list(layer_set)
     bias = synth.zipf_bias(w.E) if w.bias else None
     routers = {}
     recs = {}
     layer_s = 0.0
     layers_done = 0
-    steps = max(2, int(budget_s))
+    steps = max(4, int(budget_s * 50 / max(1, len(layer_list))) + 2)  # the budget ends the sample first
     xs = {}
     t_start = time.perf_counter()
     for step in range(steps):
-        for l in range(w.L if layers_per_step is None else layers_per_step):
+        for l in layer_list:
             if l not in routers:
                 routers[l] = synth.router_weights(w.seed, l, w.E, w.H)
                 xs[l] = np.stack([synth.hidden_ar1(w.seed, l, s, steps, w.H, w.rho) for s in range(T)], axis=1)
@@ -197,6 +219,54 @@ def cpu_sample(w, T, budget_s, layers_per_step=None, policy="lru"):
     return tokens / layer_s, layers_done, layer_s
 
 
+def _cpu_worker(job):
+    """One process of the all-core oracle sample (its own share of the layers)."""
+    import sys as _sys
+    _sys.path.insert(0, job["root"])
+    from synth.workloads import Workload
+    w = Workload(**job["workload"])
+    t0 = time.perf_counter()
+    _, layers, secs = cpu_sample(w, job["T"], job["budget"], policy=job["policy"], layer_set=job["layers"])
+    return layers, secs, time.perf_counter() - t0
+
+
+def cpu_sample_all_cores(w, T, budget_s, policy="lru"):
+    """The same oracle on every host core: one process per core (spawned, so no
+    CUDA state is inherited), each running the unchanged single-threaded oracle
+    over its own share of the layers. With one pool shared by all layers each
+    process replays the cache over its own layers only, which changes which
+    experts hit but not the oracle's work per call (routing and the unpaged
+    layer). Returns (tok/s, cores, layer calls, wall seconds)."""
+    import multiprocessing as mp
+    n = max(1, min(os.cpu_count() or 1, w.L))
+    jobs = [{"root": ROOT, "workload": dict(w.__dict__), "T": T, "budget": budget_s,
+             "policy": policy, "layers": list(range(r, w.L, n))} for r in range(n)]
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(n) as pool:
+        res = pool.map(_cpu_worker, jobs)
+    wall = time.perf_counter() - t0
+    layers = sum(r[0] for r in res)
+    busy = max(r[1] for r in res)  # the slowest process's oracle time
+    return layers * T / w.L / busy, n, layers, wall
+
+
+def cpu_baseline(w, T, budget_s, policy):
+    """The oracle on 1 host thread and on all host cores, on a bounded sample."""
+    v1, layers1, secs1 = cpu_sample(w, T, budget_s, policy=policy)
+    out = {"value": v1, "unit": "tok/s", "cores": 1, "kind": "oracle",
+           "sample": f"{layers1} layer calls ({layers1 / w.L:.2f} tokens) of the same workload, "
+                     f"{secs1:.1f} s of fp64 oracle time on 1 host thread", "nproc": os.cpu_count()}
+    try:
+        vn, n, layersn, wall = cpu_sample_all_cores(w, T, budget_s, policy)
+        out["all_cores"] = {"value": vn, "unit": "tok/s", "cores": n, "kind": "oracle",
+                            "sample": f"{layersn} layer calls over {n} processes (one per core, each the unchanged "
+                                      f"single-threaded oracle on its share of the layers), {wall:.1f} s wall"}
+    except Exception as e:  # the single-thread figure stands alone
+        out["all_cores"] = {"unavailable": str(e)[:200]}
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -208,7 +278,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     import synth
-    cache = oracle.Cache(w.L, w.E, w.pool_mode, w.slots_per_layer, oracle.slot_bytes(w.fmt, w.H, w.I),
+    cache = oracle.Cache(w.L, w.E, w.pool_mode, pool_slots(w), oracle.slot_bytes(w.fmt, w.H, w.I),
                          policy=args.eviction)
     bias = synth.zipf_bias(w.E) if w.bias else None
     total = args.warmup + args.steps
@@ -222,14 +292,14 @@ def run_reference(args):
             xs[l] = np.stack([synth.hidden_ar1(w.seed, l, s, total // w.L + 1, w.H, w.rho) for s in range(T)], axis=1)
         x = xs[l][step]
         ids, _ = oracle.topk(oracle.router_logits(x, routers[l], bias), w.k)
-        for e in np.unique(ids):
+        for e in list(np.unique(ids)) + ([-1] if w.has_shared else []):
             if (l, int(e)) not in recs:
                 recs[(l, int(e))] = synth.expert_record(w.fmt, w.seed, l, int(e), w.H, w.I)
         t0 = time.perf_counter()
         ids, _ = oracle.topk(oracle.router_logits(x, routers[l], bias), w.k)
         cache.plan(l, ids.reshape(-1), T)
         oracle.moe_layer(w.fmt, w.H, w.I, w.E, w.k, {int(e): recs[(l, int(e))] for e in np.unique(ids)}, x,
-                         routers[l], bias)
+                         routers[l], bias, shared=recs[(l, -1)] if w.has_shared else None)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             elapsed += dt
@@ -239,8 +309,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k,
-                       "format": w.fmt, "slots_per_layer": w.slots_per_layer, "eviction": args.eviction},
+            "config": bench_config(w, T, args.eviction),
             "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -292,7 +361,7 @@ def run_ours(args):
     bias = torch.from_numpy(synth.zipf_bias(w.E)).to(dev) if w.bias else None
     # the cache is primed with PRIME decode steps of the same streams before
     # the warm-up, so the timed steps see the steady-state hit rate whatever W is
-    n_total = PRIME + args.warmup + 2 * args.steps + args.profile_steps
+    n_total = PRIME + args.warmup + args.steps + args.profile_steps
     hid = np.empty((n_total, w.L, T, w.H), dtype=np.uint16)
     for l in range(w.L):
         for s in range(T):
@@ -313,8 +382,9 @@ def run_ours(args):
         x_cur.copy_(hid_dev[cursor])
         cursor += 1
 
-    # priming + warm-up (eager; also sets every kernel attribute before capture)
-    for _ in range(PRIME + args.warmup):
+    # priming (eager; also sets every kernel attribute before capture), then
+    # the capture of one step, then the warm-up steps through the graph
+    for _ in range(PRIME):
         next_inputs()
         step_layers()
     torch.cuda.synchronize()
@@ -333,6 +403,10 @@ def run_ours(args):
             graph.replay()
         else:
             step_layers()
+
+    for _ in range(args.warmup):
+        run_step()
+    torch.cuda.synchronize()
 
     s0 = cache.stats()
     clocks = ClockSampler(local)
@@ -359,11 +433,25 @@ def run_ours(args):
     up_ns = b1["upload_ns"] - b0["upload_ns"]
     value = tokens / (ms / 1e3)
 
-    # e2e: inputs from pinned host memory each step, outputs read back each step
-    e0_step = PRIME + args.warmup + args.steps
+    # e2e: the same steps from the same cache state, with each step's inputs
+    # copied in from pinned host memory and its outputs read back. The cache is
+    # reset and re-primed with the same priming and warm-up inputs (the cache is
+    # deterministic), so the window replays exactly the timed window's cache
+    # transactions, hits and misses, with the host copies added.
+    e0_step = PRIME + args.warmup
     h_in = torch.from_numpy(hid[e0_step:e0_step + args.steps].view(np.int16)).pin_memory()
     h_out = torch.empty((w.L, T, w.H), dtype=torch.float32).pin_memory()
+    cache.reset()
+    cursor = 0
+    for _ in range(PRIME):
+        next_inputs()
+        step_layers()
+    for _ in range(args.warmup):
+        run_step()
     torch.cuda.synchronize()
+    e_s0 = cache.stats()["buckets"][bk]
+    if dist:
+        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
@@ -375,8 +463,12 @@ def run_ours(args):
         h_out.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     e2e_ms, _ = aggregate(e0.elapsed_time(e1), args.steps * T, dist, dev)
-    cursor = PRIME + args.warmup + 2 * args.steps
+    e_s1 = cache.stats()["buckets"][bk]
+    e2e_same_misses = (e_s1["misses"] - e_s0["misses"]) == misses and (e_s1["hits"] - e_s0["hits"]) == hits
+    cursor = PRIME + args.warmup + args.steps
 
     # Per-launch device time of every stage, call by call over further steps of
     # the same streams: a spin kernel ahead of each call lets the host enqueue
@@ -487,22 +579,16 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
-        v, layers, secs = cpu_sample(w, T, args.cpu_seconds, policy=args.eviction)
-        cpu = {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
-               "sample": f"{layers} layer calls ({layers / w.L:.2f} tokens) of the same workload, "
-                         f"{secs:.1f} s of fp64 oracle time on 1 host thread"}
+        cpu = cpu_baseline(w, T, args.cpu_seconds, args.eviction)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": f"f16 tensor-core products ({w.fmt} weights dequantised exactly, bf16 activations), fp32 accumulate", "data": "synthetic",
-        "config": {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
-                   "inter": w.I, "format": w.fmt, "slots_per_layer": w.slots_per_layer,
-                   "pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
-                   "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
-                   "cache_priming_steps": PRIME, "eviction": args.eviction,
-                   "l2": "inputs larger than L2: each step reads ~1 GB of distinct expert bytes from an "
-                         f"{info['pool_device_bytes'] / 1e9:.1f} GB slot pool"},
+        "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+        "config": bench_config(w, T, args.eviction),
+        "run": {"pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
+                "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
+                "cache_priming_steps": PRIME, "decode_mode": args.decode},
         "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
         "topk_fp64_reranks": s1["topk_fp64_rerank"] - s0["topk_fp64_rerank"],
         "upload_gbs": up_bytes / up_ns if up_ns else None, "host_link_h2d_gbs": link_gbs,
@@ -517,7 +603,9 @@ def run_ours(args):
         "profiled_calls": len(calls), "profiled_all_hit_calls": n_hit_calls, "profiled_misses": pmiss,
         "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tok/s",
-                "h2d_bytes_per_step": w.L * T * w.H * 2, "d2h_bytes_per_step": w.L * T * w.H * 4},
+                "h2d_bytes_per_step": w.L * T * w.H * 2, "d2h_bytes_per_step": w.L * T * w.H * 4,
+                "window": "the timed window's steps replayed from the same cache state (reset and re-primed)",
+                "same_hits_and_misses": e2e_same_misses},
         "gpu_launches": int(round(launches_per_call * w.L * args.steps)) * world,
         "clocks": clk,
         "cpu_baseline": cpu,
