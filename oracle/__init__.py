@@ -19,6 +19,7 @@ _SO = os.path.join(_HERE, "liboracle.so")
 FMT = {"bf16": 0, "q4_0": 1, "fp8_b128": 2, "nvfp4": 3}
 POOL = {"per_layer": 0, "shared": 1}
 POLICY = {"lru": 0, "lfu": 1}
+PREFILL = {"read_only": 0, "page_in": 1}
 OK, ERR_INVALID, ERR_CAPACITY, ERR_MISSING = 0, 1, 2, 3
 
 _lib = None
@@ -76,6 +77,7 @@ def lib():
         L.orc_count_runs.argtypes = [vp, vp, i32]
         L.orc_wave_split.argtypes = [i32, i32, i32, vp, vp]
         L.orc_cache_set_policy.argtypes = [vp, i32]
+        L.orc_cache_set_prefill_mode.argtypes = [vp, i32]
         _lib = L
     return _lib
 
@@ -197,7 +199,8 @@ class CacheError(RuntimeError):
 class Cache:
     """The literal LRU list (moe_oracle.c), one instance per simulated cache."""
 
-    def __init__(self, L, E, pool_mode, slots_per_pool, slot_bytes=0.0, max_cache_tokens=32, policy="lru"):
+    def __init__(self, L, E, pool_mode, slots_per_pool, slot_bytes=0.0, max_cache_tokens=32, policy="lru",
+                 prefill="read_only"):
         self.L, self.E = L, E
         self.h = lib().orc_cache_create(L, E, POOL[pool_mode] if isinstance(pool_mode, str) else pool_mode,
                                         slots_per_pool, float(slot_bytes), max_cache_tokens)
@@ -205,6 +208,8 @@ class Cache:
             raise ValueError("invalid oracle cache configuration")
         if lib().orc_cache_set_policy(self.h, POLICY.get(policy, -1)) != OK:
             raise ValueError("invalid eviction policy")
+        if lib().orc_cache_set_prefill_mode(self.h, PREFILL.get(prefill, -1)) != OK:
+            raise ValueError("invalid prefill mode")
         self.n_pools = lib().orc_cache_num_pools(self.h)
         self.K = lib().orc_cache_slots(self.h)
 

@@ -381,6 +381,8 @@ struct orc_cache {
     int policy;      /* ORC_POLICY_LRU or ORC_POLICY_LFU */
     uint64_t* uses;  /* [L*E] calls that routed each key, over the whole history (LFU) */
     char* inuse;     /* [K] scratch: slots the current call holds (LFU) */
+    int prefill_mode;   /* ORC_PREFILL_READ_ONLY or ORC_PREFILL_PAGE_IN */
+    int32_t* use_slot;  /* [E] scratch: the slot an expert is read from in the current call */
 };
 
 /* Initial list: every slot empty, ordered 0..K-1 with slot 0 at the head. */
@@ -426,7 +428,9 @@ orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, dou
     c->was_hit = (char*)malloc((size_t)E);
     c->uses = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)L * E);
     c->inuse = (char*)malloc((size_t)c->K);
+    c->use_slot = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
     c->policy = ORC_POLICY_LRU;
+    c->prefill_mode = ORC_PREFILL_READ_ONLY;
     orc_cache_reset(c);
     return c;
 }
@@ -444,13 +448,37 @@ orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, dou
  * cache. */
 int orc_cache_set_policy(orc_cache* c, int policy) {
     if (!c || (policy != ORC_POLICY_LRU && policy != ORC_POLICY_LFU)) return ORC_ERR_INVALID;
+    if (policy != ORC_POLICY_LRU && c->prefill_mode == ORC_PREFILL_PAGE_IN) return ORC_ERR_INVALID;
     c->policy = policy;
     orc_cache_reset(c);
     return ORC_OK;
 }
 
+/* How a prefill call (T > max_cache_tokens) treats the cache. The pages
+ * differ [T4, "What the MoE Cache Actually Caches"; PAGED, "Why do short
+ * prompts get slower first tokens?"]:
+ *  - READ_ONLY (llama.cpp): resident experts are read in place, the others
+ *    are staged for the call only; the list does not change.
+ *  - PAGE_IN (SGLang Paged Experts): the prefill pages in every expert it
+ *    routes to that is not resident, once. Read as the decode transaction
+ *    over all of the call's distinct experts, without the capacity rule:
+ *    dedupe, touch the hits, then each miss in ascending order takes the
+ *    least recently used slot, evicting its key, and becomes the most
+ *    recently used. When the call has more distinct experts than slots, the
+ *    later misses take slots that earlier experts of the same call were read
+ *    from (so each such expert is used, and then evicted, within the call).
+ *    Needs LRU eviction (the LFU rule takes slots the call does not hold).
+ * ORC_ERR_INVALID for another value, or PAGE_IN with LFU. */
+int orc_cache_set_prefill_mode(orc_cache* c, int mode) {
+    if (!c || (mode != ORC_PREFILL_READ_ONLY && mode != ORC_PREFILL_PAGE_IN)) return ORC_ERR_INVALID;
+    if (mode == ORC_PREFILL_PAGE_IN && c->policy != ORC_POLICY_LRU) return ORC_ERR_INVALID;
+    c->prefill_mode = mode;
+    return ORC_OK;
+}
+
 void orc_cache_destroy(orc_cache* c) {
     if (!c) return;
+    free(c->use_slot);
     free(c->slot_map);
     free(c->key_of);
     free(c->prev);
@@ -524,6 +552,48 @@ int orc_cache_plan(orc_cache* c, int layer, const int32_t* ids, int n_ids, int T
         }
     }
     b = bucket_of(T);
+
+    if (T > c->max_cache_tokens && c->prefill_mode == ORC_PREFILL_PAGE_IN) {
+        /* page-in: the decode transaction over every distinct expert, with
+         * no capacity rule; slot_of is the slot each expert is read from
+         * (a hit's slot when it is touched, a miss's when it is filled) */
+        for (i = 0; i < nu; ++i) {
+            int32_t e = c->uniq[i];
+            if (smap[e] >= 0) {
+                c->use_slot[e] = smap[e];
+                lru_touch(c, p, smap[e]);
+                c->was_hit[e] = 1;
+                nh++;
+            }
+        }
+        qsort(c->uniq, (size_t)nu, sizeof(int32_t), cmp_i32);
+        for (i = 0; i < nu; ++i) {
+            int32_t e = c->uniq[i], s, old;
+            if (c->was_hit[e]) continue;
+            s = c->head[p];
+            old = c->key_of[(size_t)p * c->K + s];
+            if (old >= 0) c->slot_map[old] = -1;
+            c->key_of[(size_t)p * c->K + s] = layer * c->E + e;
+            smap[e] = s;
+            lru_touch(c, p, s);
+            c->use_slot[e] = s;
+            fill_expert[nf] = e;
+            fill_slot[nf] = s;
+            nf++;
+        }
+        for (i = 0; i < n_ids; ++i) {
+            slot_of[i] = c->use_slot[ids[i]];
+            hit_of[i] = (uint8_t)c->was_hit[ids[i]];
+        }
+        c->stats[b][0] += 1;
+        c->stats[b][1] += (uint64_t)nh;
+        c->stats[b][2] += (uint64_t)nf;
+        c->stats[b][3] += (uint64_t)((double)nf * c->slot_bytes);
+        *n_fill = nf;
+        *n_hit = nh;
+        *n_uniq = nu;
+        return ORC_OK;
+    }
 
     if (T > c->max_cache_tokens) {
         /* read-only lookup: resident experts are read in place, the rest are

@@ -45,6 +45,7 @@ enum { ORC_FMT_BF16 = 0, ORC_FMT_Q4_0 = 1, ORC_FMT_FP8_B128 = 2, ORC_FMT_NVFP4 =
 /* Pool scopes: one K-slot pool per layer [PAGED], or one pool for all layers [T4]. */
 enum { ORC_POOL_PER_LAYER = 0, ORC_POOL_SHARED = 1 };
 enum { ORC_POLICY_LRU = 0, ORC_POLICY_LFU = 1 };
+enum { ORC_PREFILL_READ_ONLY = 0, ORC_PREFILL_PAGE_IN = 1 };
 /* Status codes. */
 enum { ORC_OK = 0, ORC_ERR_INVALID = 1, ORC_ERR_CAPACITY = 2, ORC_ERR_MISSING = 3 };
 
@@ -101,7 +102,9 @@ void orc_cache_reset(orc_cache* c);
 /* One layer call of T tokens with ids[n_ids] in [token][rank] order.
  * T <= max_cache_tokens: the cache transaction (dedupe, touch hits, sorted
  *   misses take the LRU head). T > max_cache_tokens: read-only lookup (no
- *   list change); misses are staged, not cached, and slot_of is -1 for them.
+ *   list change); misses are staged, not cached, and slot_of is -1 for them;
+ *   or, in ORC_PREFILL_PAGE_IN mode, the transaction over every distinct
+ *   expert without the capacity rule (slot_of: the slot each is read from).
  * Outputs: slot_of[n_ids], hit_of[n_ids] (1 if that id's expert was resident
  * at the start of the call), fill_expert/fill_slot[n_fill], counts. Returns
  * ORC_ERR_CAPACITY (state untouched) if the unique count exceeds the pool. */
@@ -118,6 +121,9 @@ void orc_cache_stats(const orc_cache* c, uint64_t* stats);
 /* Eviction policy (ORC_POLICY_LRU, the default, or ORC_POLICY_LFU); resets the
  * cache. ORC_ERR_INVALID for another value. */
 int orc_cache_set_policy(orc_cache* c, int policy);
+/* Prefill mode (ORC_PREFILL_READ_ONLY, the default, or ORC_PREFILL_PAGE_IN,
+ * which needs LRU). ORC_ERR_INVALID otherwise. */
+int orc_cache_set_prefill_mode(orc_cache* c, int mode);
 /* The waves of a decode step of T tokens on a pool of K slots: successive
  * groups of K // k tokens; returns their number (0 if K < k). */
 int orc_wave_split(int T, int k, int K, int32_t* start, int32_t* count);
