@@ -47,6 +47,13 @@ def parse():
                     help="decode launch mode (auto: one kernel for one- or two-token calls on per-layer pools)")
     ap.add_argument("--eviction", default="lru", choices=["lru", "lfu"],
                     help="slot eviction policy of the cache (least recently / least frequently used)")
+    ap.add_argument("--chained", action="store_true",
+                    help="layer l+1's input from layer l's output (residual stream + RMS norm) instead of its own "
+                         "AR(1) stream; layer 0 takes the token's stream")
+    ap.add_argument("--speculate", action="store_true",
+                    help="speculative next-layer routing and prefetch (registers every layer's router)")
+    ap.add_argument("--clock-ms", type=float, default=100.0,
+                    help="interval of the clock and throttle-reason samples during the timed region")
     ap.add_argument("--prefill", action="store_true",
                     help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()
@@ -89,9 +96,10 @@ def pool_slots(w):
     return oracle.slots_for_budget(w.pool_bytes, oracle.slot_bytes(w.fmt, w.H, w.I))
 
 
-def bench_config(w, T, eviction):
+def bench_config(w, T, eviction, chained=False):
     """The workload a line measures; the same dict on both arms."""
     return {"workload": w.name, "batch": T, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
+            "inputs": "chained (layer l+1 from layer l's output)" if chained else "an AR(1) stream per layer",
             "inter": w.I, "format": w.fmt, "shared_expert": w.has_shared, "pool": w.pool_mode,
             "slots_per_pool": pool_slots(w), "pool_bytes": w.pool_bytes if w.pool_mode == "shared" else None,
             "eviction": eviction, "router_bias": w.bias,
@@ -114,7 +122,8 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
 
-    def __init__(self, torch_dev):
+    def __init__(self, torch_dev, interval_ms=100.0):
+        self.interval = max(0.001, interval_ms / 1e3)
         self.ok = False
         self.samples = []
         self.reasons = 0
@@ -146,7 +155,7 @@ class ClockSampler:
                 self.samples.append(c.value)
             if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
                 self.reasons |= r.value & ~0x1
-            time.sleep(0.002)
+            self._stop.wait(self.interval)
 
     def start(self):
         if not self.ok:
@@ -346,7 +355,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
-                          max_tokens=max(T, 1), device=local, decode=args.decode, eviction=args.eviction)
+                          max_tokens=max(T, 1), device=local, decode=args.decode, eviction=args.eviction,
+                          speculate=args.speculate)
     t_setup = time.perf_counter()
     cache = pec.MoECache(cfg)
     buf = None
@@ -359,6 +369,9 @@ def run_ours(args):
     routers = torch.stack([torch.from_numpy(synth.router_weights(w.seed, l, w.E, w.H).view(np.int16))
                            for l in range(w.L)]).to(dev)
     bias = torch.from_numpy(synth.zipf_bias(w.E)).to(dev) if w.bias else None
+    if args.speculate:
+        for l in range(w.L):
+            cache.set_router(l, routers[l], bias)
     # the cache is primed with PRIME decode steps of the same streams before
     # the warm-up, so the timed steps see the steady-state hit rate whatever W is
     n_total = PRIME + args.warmup + args.steps + args.profile_steps
@@ -371,9 +384,25 @@ def run_ours(args):
     out = torch.empty((w.L, T, w.H), dtype=torch.float32, device=dev)
     setup_s = time.perf_counter() - t_setup
 
+    resid = torch.empty((T, w.H), dtype=torch.float32, device=dev)
+    x_chain = torch.empty((w.L, T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def glue(l):
+        # the residual stream of a chained step: h += y_l, x_{l+1} = RMSNorm(h) in bf16
+        resid.add_(out[l])
+        x_chain[l + 1].copy_(torch.nn.functional.rms_norm(resid, (w.H,), eps=1e-6))
+
     def step_layers():
+        if not args.chained:
+            for l in range(w.L):
+                cache.forward(x_cur[l], routers[l], l, out[l], bias=bias, T=T)
+            return
+        x_chain[0].copy_(x_cur[0].view(torch.bfloat16))
+        resid.copy_(x_chain[0])
         for l in range(w.L):
-            cache.forward(x_cur[l], routers[l], l, out[l], bias=bias, T=T)
+            cache.forward(x_chain[l], routers[l], l, out[l], bias=bias, T=T)
+            if l + 1 < w.L:
+                glue(l)
 
     cursor = 0
 
@@ -409,7 +438,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     s0 = cache.stats()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_ms)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -455,7 +484,10 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        x_cur.copy_(h_in[i], non_blocking=True)
+        if args.chained:
+            x_cur[0].copy_(h_in[i][0], non_blocking=True)
+        else:
+            x_cur.copy_(h_in[i], non_blocking=True)
         if graph is not None:
             graph.replay()
         else:
@@ -482,12 +514,17 @@ def run_ours(args):
     calls = []
     for _ in range(args.profile_steps):
         next_inputs()
+        if args.chained:
+            x_chain[0].copy_(x_cur[0].view(torch.bfloat16))
+            resid.copy_(x_chain[0])
         for l in range(w.L):
             m0 = cache.stats()["buckets"][bk]["misses"]
             torch.cuda._sleep(spin_cycles)
-            cache.forward(x_cur[l], routers[l], l, out[l], bias=bias, T=T)
+            cache.forward(x_chain[l] if args.chained else x_cur[l], routers[l], l, out[l], bias=bias, T=T)
             prof = cache.profile_read()
             calls.append((cache.stats()["buckets"][bk]["misses"] - m0, prof))
+            if args.chained and l + 1 < w.L:
+                glue(l)
     cache.profile_enable(False)
     stages = ("route", "copy", "gateup", "down", "layer")
     launches_per_call = sum(sum(p[k]["launches"] for k in stages) for _, p in calls) / len(calls)
@@ -577,6 +614,29 @@ def run_ours(args):
                     "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": gu_hit,
                     "launches_averaged": n_hit_calls, "dominant_stage": dominant}
 
+    spec = None
+    if args.speculate:
+        used = s1["spec_used"] - s0["spec_used"]
+        pref = s1["spec_prefetched"] - s0["spec_prefetched"]
+        spec = {"records_prefetched": pref, "misses_read_from_bank": used, "misses": misses,
+                "share_of_misses_prefetched": used / max(1, misses), "prefetches_used": used / max(1, pref)}
+    glue_us = None
+    if args.chained:
+        # the residual glue alone (not part of the method): its own graph, timed the same way
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream if graph is not None else torch.cuda.Stream()):
+            with torch.cuda.graph(gg):
+                for l in range(w.L - 1):
+                    glue(l)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(32):
+            gg.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        glue_us = g0.elapsed_time(g1) * 1e3 / (32 * (w.L - 1))
+
     cpu = None
     if rank == 0 and args.cpu_seconds > 0:
         cpu = cpu_baseline(w, T, args.cpu_seconds, args.eviction)
@@ -585,10 +645,15 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
-        "config": bench_config(w, T, args.eviction),
+        "config": bench_config(w, T, args.eviction, args.chained),
+        "speculation": spec,
+        "chained": {"glue_us_per_layer": glue_us,
+                    "note": "layer l+1's input is RMSNorm(h) with h += layer l's output; the glue's kernels "
+                            "are inside the timed region"} if args.chained else None,
         "run": {"pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
                 "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
-                "cache_priming_steps": PRIME, "decode_mode": args.decode},
+                "cache_priming_steps": PRIME, "decode_mode": args.decode, "speculate": args.speculate,
+                "clock_sample_ms": args.clock_ms},
         "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
         "topk_fp64_reranks": s1["topk_fp64_rerank"] - s0["topk_fp64_rerank"],
         "upload_gbs": up_bytes / up_ns if up_ns else None, "host_link_h2d_gbs": link_gbs,
@@ -603,7 +668,8 @@ def run_ours(args):
         "profiled_calls": len(calls), "profiled_all_hit_calls": n_hit_calls, "profiled_misses": pmiss,
         "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tok/s",
-                "h2d_bytes_per_step": w.L * T * w.H * 2, "d2h_bytes_per_step": w.L * T * w.H * 4,
+                "h2d_bytes_per_step": (1 if args.chained else w.L) * T * w.H * 2,
+                "d2h_bytes_per_step": w.L * T * w.H * 4,
                 "window": "the timed window's steps replayed from the same cache state (reset and re-primed)",
                 "same_hits_and_misses": e2e_same_misses},
         "gpu_launches": int(round(launches_per_call * w.L * args.steps)) * world,
@@ -676,7 +742,7 @@ def run_prefill(args):
     torch.cuda.synchronize()
     s0 = cache.stats()["buckets"][2]
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(0)
+    clocks = ClockSampler(0, args.clock_ms)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.start()
     ev0.record(stream)

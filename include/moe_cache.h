@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
     MOE_OK = 0,
@@ -137,11 +137,23 @@ typedef struct {
                                  floor(slots / top_k) tokens (the last one shorter), each a cache
                                  transaction and a trace record of its own, in token order. */
     int32_t eviction;         /* moe_eviction_t (default MOE_EVICT_LRU) */
+    int32_t speculate;        /* 0 (default) or 1: speculative next-layer routing and prefetch
+                                 [NVME, "Workflow", "Evidence"]. A decode call of layer l with
+                                 T <= 2 tokens, when layer l + 1's router is registered
+                                 (moe_cache_set_router), ranks layer l + 1's experts on layer l's
+                                 input on an internal side stream and copies the predicted ones that
+                                 are not resident from the host store into a prefetch bank in device
+                                 memory, beside layer l's expert kernels. Layer l + 1's call then
+                                 reads its missed experts from the bank where they were predicted,
+                                 instead of over the host link. Speculation moves bytes only: the
+                                 routing, the cache plan, the outputs, the stats and the trace are
+                                 bitwise those of speculate = 0. Decode calls take the three-kernel
+                                 path while it is on. */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
  * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0,
- * MOE_EVICT_LRU; shape fields zero. */
+ * MOE_EVICT_LRU, speculate 0; shape fields zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {
@@ -161,6 +173,8 @@ typedef struct {
     uint64_t slot_bytes;     /* bytes one slot holds */
     uint64_t record_bytes;   /* canonical record bytes */
     uint64_t topk_fp64_rerank; /* router calls that needed the fp64 re-rank */
+    uint64_t spec_prefetched;  /* records copied into the prefetch bank by speculation */
+    uint64_t spec_used;        /* missed experts read from the prefetch bank instead of the host store */
 } moe_stats_t;
 
 typedef struct {
@@ -232,6 +246,19 @@ moe_status_t moe_cache_load_shared(moe_cache_t* h, int32_t layer, const void* re
  * call synchronises `stream`. */
 moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, const void* router_w,
                                const float* router_bias, int32_t layer_id, float* out, void* stream);
+
+/* Registers the router of `layer` for speculative routing (speculate = 1):
+ * router_w device bf16 [E x H], router_bias device fp32 [E] or NULL, the
+ * same buffers the caller passes to moe_layer_forward for that layer. The
+ * caller keeps them alive and unchanged until it registers others or
+ * destroys the handle; router_w NULL unregisters the layer. Speculation for
+ * layer l + 1 runs only while its router is registered [NVME, "Workflow":
+ * run the next layer's router on the current layer's input].
+ * The side stream's work for layer l + 1 is ordered before layer l + 1's
+ * expert kernels (and before any other layer's call) on the caller's stream,
+ * so a stream that issues the layers in order, up to the last, holds no
+ * side-stream work afterwards. MOE_ERR_INVALID for a bad layer. */
+moe_status_t moe_cache_set_router(moe_cache_t* h, int32_t layer, const void* router_w, const float* router_bias);
 
 /* Synchronises the device and copies the counters out. Returns
  * MOE_ERR_TIMEOUT (counters still copied) if a grid barrier of the one-kernel

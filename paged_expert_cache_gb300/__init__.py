@@ -33,7 +33,7 @@ class MoeConfig(ctypes.Structure):
                 ("format", i32), ("has_shared", i32), ("pool_mode", i32), ("slots_per_layer", i32),
                 ("upload_mode", i32), ("pool_bytes", dbl), ("norm_topk", i32), ("max_cache_tokens", i32),
                 ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32),
-                ("multi_wave", i32), ("eviction", i32)]
+                ("multi_wave", i32), ("eviction", i32), ("speculate", i32)]
 
 
 class BucketStats(ctypes.Structure):
@@ -42,7 +42,7 @@ class BucketStats(ctypes.Structure):
 
 class MoeStats(ctypes.Structure):
     _fields_ = [("bucket", BucketStats * 3), ("num_pools", i32), ("slots_per_pool", i32), ("slot_bytes", u64),
-                ("record_bytes", u64), ("topk_fp64_rerank", u64)]
+                ("record_bytes", u64), ("topk_fp64_rerank", u64), ("spec_prefetched", u64), ("spec_used", u64)]
 
 
 class MoeInfo(ctypes.Structure):
@@ -92,6 +92,7 @@ def load():
         "moe_cache_profile_enable": (i32, [vp, i32]),
         "moe_cache_profile_read": (i32, [vp, P(MoeProfile)]),
         "moe_route_topk_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
+        "moe_cache_set_router": (i32, [vp, i32, vp, vp]),
         "moe_cache_reset": (i32, [vp]),
         "moe_cache_destroy": (i32, [vp]),
     }
@@ -124,7 +125,7 @@ def _check(st, handle=None):
 
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
-                max_tokens=32, device=0, decode="auto", multi_wave=False, eviction="lru"):
+                max_tokens=32, device=0, decode="auto", multi_wave=False, eviction="lru", speculate=False):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -142,6 +143,7 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.split_decode = DECODE_MODES[decode] if isinstance(decode, str) else int(decode)
     c.multi_wave = 1 if multi_wave else 0
     c.eviction = EVICTIONS[eviction] if isinstance(eviction, str) else int(eviction)
+    c.speculate = 1 if speculate else 0
     return c
 
 
@@ -273,12 +275,19 @@ class MoECache:
                                         stream or None), self.h)
         return out
 
+    def set_router(self, layer, router_w, bias=None):
+        """moe_cache_set_router: registers layer's router (device bf16 [E, H],
+        device fp32 [E] or None) for speculative next-layer routing; the
+        tensors must stay alive and unchanged while registered."""
+        _check(load().moe_cache_set_router(self.h, layer, _ptr(router_w), _ptr(bias)), self.h)
+
     def stats(self):
         s = MoeStats()
         _check(load().moe_cache_stats(self.h, ctypes.byref(s)), self.h)
         buckets = [{f: getattr(s.bucket[b], f) for f, _ in BucketStats._fields_} for b in range(3)]
         return {"buckets": buckets, "num_pools": s.num_pools, "slots_per_pool": s.slots_per_pool,
-                "slot_bytes": s.slot_bytes, "record_bytes": s.record_bytes, "topk_fp64_rerank": s.topk_fp64_rerank}
+                "slot_bytes": s.slot_bytes, "record_bytes": s.record_bytes, "topk_fp64_rerank": s.topk_fp64_rerank,
+                "spec_prefetched": s.spec_prefetched, "spec_used": s.spec_used}
 
     def info(self):
         s = MoeInfo()

@@ -46,6 +46,16 @@ struct moe_cache {
     cudaEvent_t ev_plan = nullptr, ev_copy[2] = {nullptr, nullptr}, ev_gemm[2] = {nullptr, nullptr};
     struct Span { int stage, a, b; };
     std::vector<Span> spans;
+    // speculative next-layer routing: the registered routers, the side stream,
+    // its events per layer parity and the layer whose prefetch is in flight
+    std::vector<const void*> spec_w;
+    std::vector<const float*> spec_b;
+    cudaStream_t spec_stream = nullptr;
+    cudaEvent_t ev_route[2] = {nullptr, nullptr}, ev_spec_plan[2] = {nullptr, nullptr},
+                ev_spec_copy[2] = {nullptr, nullptr};
+    float* spec_z = nullptr;
+    unsigned* spec_done = nullptr;
+    int spec_pending = -1;
 };
 
 namespace {
@@ -106,6 +116,13 @@ void free_all(moe_cache_t* h) {
     }
     if (h->stage_stream) cudaStreamDestroy(h->stage_stream);
     h->stage_stream = nullptr;
+    for (int i = 0; i < 2; ++i)
+        for (cudaEvent_t* e : {&h->ev_route[i], &h->ev_spec_plan[i], &h->ev_spec_copy[i]}) {
+            if (*e) cudaEventDestroy(*e);
+            *e = nullptr;
+        }
+    if (h->spec_stream) cudaStreamDestroy(h->spec_stream);
+    h->spec_stream = nullptr;
     for (void* p : h->dev_allocs) cudaFree(p);
     h->dev_allocs.clear();
     if (h->store_host) cudaFreeHost(h->store_host);
@@ -125,7 +142,12 @@ moe_status_t init_tables(moe_cache_t* h) {
     CK(h, cudaMemcpy(d.key_of, ko.data(), ko.size() * sizeof(int), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.last_use, lu.data(), lu.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.clock, clk.data(), clk.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
-    CK(h, cudaMemset(d.stats, 0, 16 * sizeof(unsigned long long)));
+    CK(h, cudaMemset(d.stats, 0, 18 * sizeof(unsigned long long)));
+    if (d.bank_n) {
+        CK(h, cudaMemset(d.bank_n, 0, 2 * sizeof(int)));
+        CK(h, cudaMemset(d.bank_key, 0xff, 2 * (size_t)d.bank_half * sizeof(int)));
+    }
+    h->spec_pending = -1;
     CK(h, cudaMemset(d.uses, 0, (size_t)d.L * d.E * sizeof(unsigned)));
     if (h->scr.grid_bar) CK(h, cudaMemset(h->scr.grid_bar, 0, sizeof(unsigned)));
     if (h->scr.err) CK(h, cudaMemset(h->scr.err, 0, sizeof(unsigned)));
@@ -155,6 +177,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->split_decode = MOE_DECODE_AUTO;
     cfg->multi_wave = 0;
     cfg->eviction = MOE_EVICT_LRU;
+    cfg->speculate = 0;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -187,6 +210,9 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     if (c.multi_wave != 0 && c.multi_wave != 1) return fail(nullptr, MOE_ERR_INVALID, "multi_wave must be 0 or 1");
     if (c.eviction != MOE_EVICT_LRU && c.eviction != MOE_EVICT_LFU)
         return fail(nullptr, MOE_ERR_INVALID, "unknown eviction policy");
+    if (c.speculate != 0 && c.speculate != 1) return fail(nullptr, MOE_ERR_INVALID, "speculate must be 0 or 1");
+    if (c.speculate && c.upload_mode != MOE_UPLOAD_PULL)
+        return fail(nullptr, MOE_ERR_INVALID, "speculation needs MOE_UPLOAD_PULL");
     if (c.max_cache_tokens < 1 || c.max_cache_tokens > moe::kDecodeMaxTokens)
         return fail(nullptr, MOE_ERR_INVALID, "max_cache_tokens must be in 1..32");
     if (c.max_tokens < 1) return fail(nullptr, MOE_ERR_INVALID, "max_tokens must be >= 1");
@@ -271,7 +297,27 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(d.clock, (size_t)d.n_pools);
     DA(d.uses, (size_t)d.L * d.E);
     d.lfu = c.eviction == MOE_EVICT_LFU ? 1 : 0;
-    DA(d.stats, 16);
+    DA(d.stats, 18);
+    h->spec_w.assign(d.L, nullptr);
+    h->spec_b.assign(d.L, nullptr);
+    if (c.speculate) {
+        // the prefetch bank: two halves (layer parity) of top_k x kSpecMaxTokens slots
+        d.bank_half = d.k * moe::kSpecMaxTokens;
+        uint8_t* bank = nullptr;
+        DA(bank, 2 * (size_t)d.bank_half * h->slot_stride);
+        d.bank = bank;
+        DA(d.bank_key, 2 * (size_t)d.bank_half);
+        DA(d.bank_n, 2);
+        DA(h->spec_z, (size_t)moe::kSpecMaxTokens * d.E);
+        DA(h->spec_done, 1);
+        if (cudaMemset(h->spec_done, 0, 4) != cudaSuccess) return bail(MOE_ERR_CUDA, "scratch initialisation failed");
+        if (cudaStreamCreateWithFlags(&h->spec_stream, cudaStreamNonBlocking) != cudaSuccess)
+            return bail(MOE_ERR_CUDA, "speculation stream creation failed");
+        for (int i = 0; i < 2; ++i)
+            for (cudaEvent_t* ev : {&h->ev_route[i], &h->ev_spec_plan[i], &h->ev_spec_copy[i]})
+                if (cudaEventCreateWithFlags(ev, cudaEventDisableTiming) != cudaSuccess)
+                    return bail(MOE_ERR_CUDA, "speculation event creation failed");
+    }
     DA(d.trace_count, 1);
     d.trace = nullptr;
     d.trace_cap = 0;
@@ -381,6 +427,12 @@ moe_status_t moe_cache_load_experts(moe_cache_t* h, int32_t layer, int32_t first
         uint8_t& f = h->loaded[(size_t)layer * d.E + first + i];
         if (!f) { f = 1; h->n_loaded++; }
     }
+    if (d.bank_n) {
+        // records may have changed: nothing prefetched before stays valid
+        CK(h, cudaDeviceSynchronize());
+        CK(h, cudaMemset(d.bank_n, 0, 2 * sizeof(int)));
+        h->spec_pending = -1;
+    }
     return MOE_OK;
 }
 
@@ -427,7 +479,7 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         return MOE_OK;
     }
     const int bucket = T <= 8 ? 0 : (T <= 32 ? 1 : 2);
-    moe::RouteArgs a;
+    moe::RouteArgs a = {};
     a.x = (const uint16_t*)hidden;
     a.w = (const uint16_t*)router_w;
     a.bias = router_bias;
@@ -442,6 +494,22 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     a.early = (d.pool_mode == 0 && h->last_layer >= 0 && h->last_layer != layer_id) ? 1 : 0;
     h->last_layer = layer_id;
     const int units = std::min(T * d.k, d.E) + d.has_shared;
+    // Speculation: the side stream's prefetch for layer spec_pending. Its bank
+    // keys are ordered before this call's routing; when it was made for this
+    // call, its copies are ordered before this call's expert kernels (below),
+    // otherwise before everything of this call.
+    bool use_bank = false;
+    if (h->spec_pending >= 0) {
+        const int half = h->spec_pending & 1;
+        CK(h, cudaStreamWaitEvent(st, h->ev_spec_plan[half], 0));
+        if (h->spec_pending == layer_id && decode && T <= moe::kSpecMaxTokens) {
+            use_bank = true;
+        } else {
+            CK(h, cudaStreamWaitEvent(st, h->ev_spec_copy[half], 0));
+            h->spec_pending = -1;
+        }
+    }
+    a.spec = use_bank ? 1 : 0;
     // programmatic dependent launch between the decode kernels (off while
     // events bracket each launch for profiling)
     const bool pdl = !h->prof_on;
@@ -454,7 +522,9 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     // boundaries saved
     const int mode = h->cfg.split_decode;
     const bool one_kernel_pays = mode == MOE_DECODE_ONE_KERNEL || (T <= 2 && d.pool_mode == MOE_POOL_PER_LAYER);
-    if (decode && mode != MOE_DECODE_THREE_KERNELS && one_kernel_pays && h->fused_ok &&
+    // the side stream's kernels run beside the expert kernels, so speculation
+    // takes the three-kernel path (the persistent kernel needs every SM)
+    if (decode && mode != MOE_DECODE_THREE_KERNELS && one_kernel_pays && h->fused_ok && !h->cfg.speculate &&
         h->cfg.upload_mode == MOE_UPLOAD_PULL && moe::layer_smem_bytes(d, T) > 0) {
         // the whole call in one persistent kernel
         timed(h, 6, st, [&] { fused = moe::launch_layer(d, h->scr, a, out, bucket, st, pdl); });
@@ -471,6 +541,34 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         // PULL: misses are pulled over the host link by the gate/up kernel,
         // which streams each missed record into its slot while it consumes it
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, pdl); });
+        if (use_bank) {
+            // this call's prefetched records must have landed before its expert kernels read them
+            CK(h, cudaStreamWaitEvent(st, h->ev_spec_copy[layer_id & 1], 0));
+            h->spec_pending = -1;
+        }
+        if (h->cfg.speculate && T <= moe::kSpecMaxTokens && layer_id + 1 < d.L && h->spec_w[layer_id + 1]) {
+            // the next layer's router on this call's tokens, on the side
+            // stream after this call's routing (its plan and everything
+            // before it), then the predicted non-resident records into the
+            // bank half of the next layer, beside this call's expert kernels
+            const int nl = layer_id + 1, half = nl & 1;
+            CK(h, cudaEventRecord(h->ev_route[half], st));
+            CK(h, cudaStreamWaitEvent(h->spec_stream, h->ev_route[half], 0));
+            moe::SpecArgs sa;
+            sa.x = a.x;
+            sa.w = (const uint16_t*)h->spec_w[nl];
+            sa.bias = h->spec_b[nl];
+            sa.T = T;
+            sa.layer = nl;
+            sa.half = half;
+            sa.z = h->spec_z;
+            sa.done = h->spec_done;
+            moe::launch_spec_route(d, sa, h->spec_stream);
+            CK(h, cudaEventRecord(h->ev_spec_plan[half], h->spec_stream));
+            moe::launch_spec_copy(d, half, h->spec_stream);
+            CK(h, cudaEventRecord(h->ev_spec_copy[half], h->spec_stream));
+            h->spec_pending = nl;
+        }
         if (h->cfg.upload_mode == MOE_UPLOAD_MEMCPY) {
             // read the fill list back, then one copy per merged run
             int* hf = h->host_fill;
@@ -544,11 +642,19 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     return MOE_OK;
 }
 
+moe_status_t moe_cache_set_router(moe_cache_t* h, int32_t layer, const void* router_w, const float* router_bias) {
+    if (!h) return fail(nullptr, MOE_ERR_INVALID, "handle is NULL");
+    if (layer < 0 || layer >= h->dev.L) return fail(h, MOE_ERR_INVALID, "layer out of range");
+    h->spec_w[layer] = router_w;
+    h->spec_b[layer] = router_w ? router_bias : nullptr;
+    return MOE_OK;
+}
+
 moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out) {
     if (!h || !out) return fail(h, MOE_ERR_INVALID, "NULL argument");
     CK(h, cudaSetDevice(h->cfg.device));
     CK(h, cudaDeviceSynchronize());
-    unsigned long long st[16];
+    unsigned long long st[18];
     CK(h, cudaMemcpy(st, h->dev.stats, sizeof st, cudaMemcpyDeviceToHost));
     memset(out, 0, sizeof(*out));
     for (int b = 0; b < 3; ++b) {
@@ -563,6 +669,8 @@ moe_status_t moe_cache_stats(moe_cache_t* h, moe_stats_t* out) {
     out->slot_bytes = h->slot_bytes;
     out->record_bytes = h->record_bytes;
     out->topk_fp64_rerank = st[15];
+    out->spec_prefetched = st[16];
+    out->spec_used = st[17];
     unsigned derr = 0;
     CK(h, cudaMemcpy(&derr, h->scr.err, sizeof derr, cudaMemcpyDeviceToHost));
     if (derr & 1u) return fail(h, MOE_ERR_TIMEOUT, "a grid barrier of the one-kernel decode path timed out");

@@ -121,7 +121,13 @@ struct CacheDev {
     unsigned long long* clock;     // [n_pools]
     unsigned* uses;                // [L*E] decode calls that routed each key (LFU)
     int lfu;                       // 1: least frequently used eviction
-    unsigned long long* stats;     // [3][5] + [15] re-rank count
+    unsigned long long* stats;     // [3][5], [15] re-rank count, [16] records prefetched by speculation,
+                                   // [17] misses read from the prefetch bank
+    uint8_t* bank;                 // speculation's prefetch bank: [2 halves][bank_half] slots, or null
+    int* bank_key;                 // [2][bank_half]: layer * E + expert of each bank slot, or -1
+    int* bank_n;                   // [2]: bank slots filled in each half
+    int bank_half;                 // bank slots per half (layer parity)
+    int pagein;                    // 1: prefill calls page their missed experts into the pool (LRU)
     int* trace;                    // ring of records, or null
     unsigned long long* trace_count;
     int trace_cap, trace_stride;
@@ -278,11 +284,18 @@ struct RouteArgs {
     int T, layer, prefill, bucket;
     int early;           // 1: no call still in flight can write this layer's pool state, so a decode
                          // kernel may read it before waiting on the preceding grid
+    int spec;            // 1: the bank half of this layer holds a speculative prefetch made for this
+                         // call, complete before its expert kernels run (misses found there read it)
 };
 
 void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int max_units, cudaStream_t st, bool pdl);
 void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
 void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st);
+// Page-in prefill: the cache transaction of a prefill call (after its plan),
+// and the copies of the paged-in records that stay resident, from the arena
+// into their slots, after the GEMMs of their staging group.
+void launch_pagein(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
+void launch_pagein_copy(const CacheDev& c, const Scratch& s, int layer, int group, int G, cudaStream_t st);
 void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st,
                  bool beside_compute);
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,
@@ -326,6 +339,21 @@ size_t gemm_max_items(int P, int Y);
 void launch_gemm(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G, int Y,
                  cudaStream_t st);
 void launch_combine(const CacheDev& c, const Scratch& s, float* out, int T, cudaStream_t st);
+
+// Speculative next-layer routing and prefetch (spec.cu): the next layer's
+// router on the current layer's tokens, its predicted non-resident experts
+// written to the bank half of that layer, then their records copied there.
+struct SpecArgs {
+    const uint16_t* x;   // [T][H] bf16: the current layer's tokens
+    const uint16_t* w;   // [E][H] bf16: the next layer's router
+    const float* bias;   // [E] or null
+    int T, layer, half;  // layer: the next layer; half: its bank half
+    float* z;            // [T][E] fp32 logits scratch
+    unsigned* done;      // CTA counter
+};
+constexpr int kSpecMaxTokens = 2;  // decode calls with at most this many tokens speculate
+void launch_spec_route(const CacheDev& c, const SpecArgs& a, cudaStream_t st);
+void launch_spec_copy(const CacheDev& c, int half, cudaStream_t st);
 
 // Host-side repack of canonical records into the slot layout (repack.cpp).
 void repack_record(int fmt, int H, int I, const uint8_t* canonical, uint8_t* slot, float* gscales3);

@@ -114,7 +114,9 @@ __host__ __device__ inline LayerLayout layer_layout(int fmt, int E, int K, int k
     L.wr = p; p = align16(p + (size_t)rows * H * 2);
     L.plan = p; p = align16(p + plan_layout(nullptr, E, K, n_ids, U, P).bytes);
     L.topk = p; p = align16(p + (size_t)(T < kLayerRankWarps ? T : kLayerRankWarps) * topk_bytes_per_warp(E));
-    L.rk = p; p = align16(p + (size_t)E * 8 + (size_t)kMaxTopK * 8);  // rank keys, picks' lower bounds (one token)
+    // one token: the rank keys (E <= 256) or the warps' sorted lists, then the picks' lower bounds
+    L.rk = p; p = align16(p + (size_t)(E > kLThreads / 32 * kMaxTopK ? E : kLThreads / 32 * kMaxTopK) * 8 +
+                          (size_t)kMaxTopK * 8);
     const size_t phase12 = p - a0;
     // region B: gate/up partials, or the down staging
     const size_t ld = (size_t)I + 8;
@@ -525,8 +527,9 @@ __device__ __forceinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, i
     return r;
 }
 
-// kOneToken: the instantiation for one token and at most 256 experts, with
-// the many-token ranking left out (its registers would crowd the rest).
+// kOneToken: the instantiation for one token and at most kLThreads (512)
+// experts, one per thread, with the many-token ranking left out (its
+// registers would crowd the rest).
 template <int FMT, bool kOneToken>
 __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
                                                       const __grid_constant__ RouteArgs a, float* __restrict__ out) {
@@ -698,10 +701,16 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
 
     // ---- 2. top-k and plan in every CTA ----------------------------------
     if (kOneToken) {
-        // one token: every expert ranked at once by its own thread
+        // one token: every expert's key held by its own thread, ranked by
+        // rounds in every warp at once and one merge
         const TopkSmem tw = topk_layout(smem + L.topk, E);
-        topk_rank_block(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
-                        reinterpret_cast<float2*>(smem + L.rk + (size_t)E * 8), &rerank, sids, swts);
+        if (E <= 256)
+            topk_rank_block(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
+                            reinterpret_cast<float2*>(smem + L.rk + (size_t)E * 8), &rerank, sids, swts);
+        else
+            topk_block_rounds(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
+                              reinterpret_cast<float2*>(smem + L.rk + (size_t)(kLThreads / 32) * kMaxTopK * 8),
+                              &rerank, sids, swts);
     } else {
         const int nrw = min(T, kLayerRankWarps);
         if (warp < nrw) {
@@ -1057,7 +1066,7 @@ static bool layer_launch_as(const CacheDev& c, const Scratch& s, const RouteArgs
 template <int FMT>
 static bool layer_launch(const CacheDev& c, const Scratch& s, const RouteArgs& a, float* out, size_t sm,
                          cudaStream_t st, bool pdl) {
-    if (a.T == 1 && c.E <= 256) return layer_launch_as<FMT, true>(c, s, a, out, sm, st, pdl);
+    if (a.T == 1 && c.E <= kLThreads) return layer_launch_as<FMT, true>(c, s, a, out, sm, st, pdl);
     return layer_launch_as<FMT, false>(c, s, a, out, sm, st, pdl);
 }
 

@@ -180,11 +180,12 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
         const int st = s.units[u].pstart, n = s.units[u].np;
         for (int j = 0; j < 8; ++j) s.units[u].pair8[j] = j < n ? s.unit_pairs[st + j] : -1;
     }
-    for (int i = tid; i < n_ids; i += nthr) {
-        int e = s.ids[i];
-        s.slot_of[i] = slot_map[e];
-        s.hit_of[i] = slot_map[e] >= 0;
-    }
+    if (!c.pagein)
+        for (int i = tid; i < n_ids; i += nthr) {
+            int e = s.ids[i];
+            s.slot_of[i] = slot_map[e];
+            s.hit_of[i] = slot_map[e] >= 0;
+        }
     __syncthreads();
     if (tid == 0) {
         Plan* pl = s.plan;
@@ -193,12 +194,184 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
         pl->n_fill = nu - nh;
         pl->n_units = n_units;
         pl->status = 0;
+        if (c.pagein) return;  // k_pagein commits the transaction, the stats and the trace
         unsigned long long* st = c.stats + a.bucket * 5;
         st[0] += 1;
         st[1] += (unsigned long long)nh;
         st[2] += (unsigned long long)(nu - nh);
         st[3] += (unsigned long long)(nu - nh) * c.slot_bytes;
         if (c.trace) write_trace(c, s, layer, T, n_ids, nh, nu - nh, nu);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Page-in prefill: "Running an MoE Model Larger Than Your VRAM: SGLang Paged
+// Experts, ..." (dev.to), "Why do short prompts get slower first tokens?": a
+// prefill pages in every expert it routes to that is not resident, once. The
+// cache transaction of decode over all of the call's distinct experts, with
+// no capacity rule: the hits are touched in first-occurrence order, then each
+// miss, in ascending expert order, takes the least recently used slot and
+// becomes the most recently used. With the last-use clock that is: the list
+// at the start of the misses is L0 = the untouched slots by ascending stamp,
+// then the hits in touch order, and miss j takes slot L0[j mod K] (from the
+// K-th miss on, a slot the same call filled or read; only the last miss
+// placed in a slot stays). One CTA, after k_plan_prefill (whose units are the
+// hits ascending, then the misses ascending). The records still cross the
+// host link once, into the staging arena; k_pagein_copy moves those that stay
+// resident from the arena into their slots after the GEMMs of their group.
+// ---------------------------------------------------------------------------
+constexpr int kPageinThreads = 1024;
+
+static size_t pagein_sort_len(int K) {
+    size_t n = 1;
+    while (n < (size_t)K) n <<= 1;
+    return n;
+}
+
+static size_t pagein_smem(const CacheDev& c) {
+    return pagein_sort_len(c.K) * 8 + (size_t)c.K * 4 + (size_t)c.E * 12 + (size_t)c.K * 4;
+}
+
+__global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s, RouteArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait();
+    const int E = c.E, K = c.K, k = c.k, layer = a.layer;
+    const int pool = c.pool_mode ? 0 : layer;
+    const int n_ids = a.T * k;
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const Plan* pl = s.plan;
+    const int nu = pl->n_uniq, nh = pl->n_hit, nm = nu - nh;
+    const size_t N = pagein_sort_len(K);
+    unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);  // [N] sort keys
+    int* L0 = reinterpret_cast<int*>(smem + N * 8);                        // [K]
+    int* first = L0 + K;                                                    // [E] first occurrence
+    int* use_slot = first + E;                                              // [E] slot read from
+    int* is_hit = use_slot + E;                                             // [E]
+    int* hit_slot = is_hit + E;                                             // [K] 1: a hit's slot
+    unsigned long long* g_lu = c.last_use + (size_t)pool * K;
+    int* g_kof = c.key_of + (size_t)pool * K;
+    int* g_smap = c.slot_map + (size_t)layer * E;
+    __shared__ unsigned long long clk;
+    if (tid == 0) clk = c.clock[pool];
+    for (int e = tid; e < E; e += nthr) {
+        first[e] = 0x7fffffff;
+        is_hit[e] = 0;
+        use_slot[e] = -1;
+    }
+    for (int i = tid; i < K; i += nthr) hit_slot[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_ids; i += nthr) atomicMin(&first[s.ids[i]], i);
+    for (int u = tid; u < nh; u += nthr) {
+        const UnitDesc& d = s.units[u];
+        is_hit[d.expert] = 1;
+        use_slot[d.expert] = d.slot;
+        hit_slot[d.slot] = 1;
+    }
+    __syncthreads();
+    // the untouched slots by ascending last-use stamp (stamps < 2^50, slots < 2^14)
+    for (size_t i = tid; i < N; i += nthr)
+        key[i] = (i < (size_t)K && !hit_slot[i]) ? ((g_lu[i] << 14) | (unsigned long long)i) : ~0ull;
+    __syncthreads();
+    for (size_t size = 2; size <= N; size <<= 1)
+        for (size_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (size_t i = tid; i < N; i += nthr) {
+                const size_t j = i ^ stride;
+                if (j > i) {
+                    const unsigned long long x = key[i], y = key[j];
+                    if ((x > y) == ((i & size) == 0)) {
+                        key[i] = y;
+                        key[j] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (int i = tid; i < K - nh; i += nthr) L0[i] = (int)(key[i] & 0x3fffull);
+    // then the hits in touch order (first occurrence), stamped clk + rank
+    for (int u = tid; u < nh; u += nthr) {
+        const UnitDesc& d = s.units[u];
+        int rank = 0;
+        for (int v = 0; v < nh; ++v) rank += first[s.units[v].expert] < first[d.expert];
+        L0[K - nh + rank] = d.slot;
+    }
+    __syncthreads();
+    // misses: miss j (ascending, staged unit nh + j) is read from slot L0[j mod K]
+    for (int j = tid; j < nm; j += nthr) {
+        const int e = s.units[nh + j].expert;
+        const int sl = L0[j % K];
+        use_slot[e] = sl;
+        s.copy_slot[j] = sl;
+    }
+    // evict what the positions that take a miss held before the call
+    const int npos = nm < K ? nm : K;
+    for (int i = tid; i < npos; i += nthr) {
+        const int old = g_kof[L0[i]];
+        if (old >= 0) c.slot_map[old] = -1;
+    }
+    __syncthreads();
+    // the last miss placed at each position stays; the hits not displaced keep
+    // their touch stamps
+    for (int i = tid; i < npos; i += nthr) {
+        const int jl = i + K * ((nm - 1 - i) / K);
+        const int e = s.units[nh + jl].expert;
+        const int sl = L0[i];
+        g_kof[sl] = layer * E + e;
+        g_smap[e] = sl;
+        g_lu[sl] = clk + nh + jl;
+    }
+    for (int r = tid; r < nh; r += nthr)
+        if (K - nh + r >= npos) g_lu[L0[K - nh + r]] = clk + r;
+    for (int i = tid; i < n_ids; i += nthr) {
+        const int e = s.ids[i];
+        s.slot_of[i] = use_slot[e];
+        s.hit_of[i] = is_hit[e];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        c.clock[pool] = clk + nh + nm;
+        unsigned long long* st = c.stats + a.bucket * 5;
+        st[0] += 1;
+        st[1] += (unsigned long long)nh;
+        st[2] += (unsigned long long)nm;
+        st[3] += (unsigned long long)nm * c.slot_bytes;
+        if (c.trace) write_trace(c, s, layer, a.T, n_ids, nh, nm, nu);
+    }
+}
+
+// Copies the paged-in records of staging group `group` that stay resident
+// (miss j stays when no later miss of the call takes its slot: j >= nm - K)
+// from the arena into their slots.
+constexpr uint64_t kPageinChunk = 32768;
+__global__ void __launch_bounds__(256) k_pagein_copy(CacheDev c, Scratch s, int layer, int group, int G) {
+    griddep_wait();
+    const Plan* pl = s.plan;
+    const int nm = pl->n_uniq - pl->n_hit;
+    const int keep_from = nm - (nm < c.K ? nm : c.K);
+    const int j0 = max(group * G, keep_from), j1 = min(group * G + G, nm);
+    if (j0 >= j1) return;
+    const int pool = c.pool_mode ? 0 : layer;
+    const uint64_t bytes = c.slot_bytes;
+    const int cpr = (int)((bytes + kPageinChunk - 1) / kPageinChunk);
+    const long long total = (long long)(j1 - j0) * cpr;
+    for (long long w = blockIdx.x; w < total; w += gridDim.x) {
+        const int j = j0 + (int)(w / cpr), ch = (int)(w % cpr);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(s.copy_dst[j]) + (size_t)ch * kPageinChunk;
+        uint8_t* dst = c.pool + ((size_t)pool * c.K + s.copy_slot[j]) * c.slot_stride + (size_t)ch * kPageinChunk;
+        const uint64_t rem = bytes - (uint64_t)ch * kPageinChunk;
+        const int nv = (int)((rem < kPageinChunk ? rem : kPageinChunk) / 16);
+        for (int v0 = threadIdx.x; v0 < nv; v0 += 256 * 8) {
+            uint4 buf[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int v = v0 + i * 256;
+                if (v < nv) buf[i] = __ldcg(reinterpret_cast<const uint4*>(src) + v);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int v = v0 + i * 256;
+                if (v < nv) reinterpret_cast<uint4*>(dst)[v] = buf[i];
+            }
+        }
     }
 }
 
@@ -244,6 +417,23 @@ void launch_topk_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a
         set_topk = sm;
     }
     k_topk<<<(a.T + kRouteWarps - 1) / kRouteWarps, kRouteThreads, sm, st>>>(c, s, a);
+}
+
+void launch_pagein(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st) {
+    const size_t sm = pagein_smem(c);
+    static size_t set = 0;
+    if (sm > set) {
+        cudaFuncSetAttribute(k_pagein, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        set = sm;
+    }
+    k_pagein<<<1, kPageinThreads, sm, st>>>(c, s, a);
+}
+
+void launch_pagein_copy(const CacheDev& c, const Scratch& s, int layer, int group, int G, cudaStream_t st) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    k_pagein_copy<<<sms > 0 ? sms : 148, 256, 0, st>>>(c, s, layer, group, G);
 }
 
 void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a, int group, cudaStream_t st) {
@@ -370,7 +560,7 @@ extern "C" moe_status_t moe_route_topk_noalloc(const void* hidden, int32_t T, co
     s.route_done = reinterpret_cast<unsigned*>(base + moe::kNoAllocLogitBytes + moe::kNoAllocBoundBytes);
     s.ids = ids;
     s.wts = weights;
-    moe::RouteArgs a;
+    moe::RouteArgs a = {};
     a.x = (const uint16_t*)hidden;
     a.w = (const uint16_t*)router_w;
     a.bias = router_bias;

@@ -601,6 +601,95 @@ static __device__ __forceinline__ void topk_token_fast(const CacheDev& c, const 
 }
 
 
+// The largest of the lanes' 64-bit keys (all distinct, or zero): the high
+// words by one reduction, then, where several lanes tie there, the low words
+// among the tied lanes. Every lane of the warp calls it and gets the key.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long key) {
+    const unsigned hi = (unsigned)(key >> 32);
+    const unsigned mhi = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned tied = __ballot_sync(0xffffffffu, hi == mhi);
+    if (__popc(tied) == 1) return __shfl_sync(0xffffffffu, key, __ffs(tied) - 1);
+    const unsigned lo = hi == mhi ? (unsigned)key : 0u;
+    return ((unsigned long long)mhi << 32) | __reduce_max_sync(0xffffffffu, lo);
+}
+
+// Top-k of token 0 by the whole CTA (E <= blockDim.x, k <= kMaxTopK): thread e
+// builds expert e's key (the orderable 64-bit key of topk_token_fast: the
+// logit's high part, then its low part with 1023 - e in the low bits, so keys
+// are distinct). Each warp takes the k largest keys of its 32 experts by k
+// rounds of a warp-wide maximum, in order, into wl [warps][kMaxTopK]; warp 0
+// then merges the warps' sorted lists by k rounds of a maximum over the
+// lists' heads. The picks are the k largest keys in descending order, those
+// of the sorted-list rounds. The certificate is topk_token_fast's (each pick's
+// lower bound above the upper bound of everything ranked after it), checked by
+// every expert against the picks ranked above it and combined with one
+// block-wide AND; warp 0 then weighs as topk_token_fast does, or re-ranks
+// exactly. Every thread of the CTA calls it; lowb: k entries of shared memory.
+static __device__ void topk_block_rounds(const CacheDev& c, const Scratch& s, const RouteArgs& a, const TopkSmem& w,
+                                         unsigned long long* wl, float2* lowb, int* rerank_flag, int* ids_out,
+                                         float* wts_out) {
+    const int E = c.E, k = c.k, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nw = (int)(blockDim.x >> 5);
+    unsigned long long key = 0ull;
+    if (tid < E) {
+        const float2 z = __ldcg(s.logits + tid);
+        w.z[tid] = z;
+        w.b[tid] = __ldcg(s.bounds + tid);
+        key = ((unsigned long long)ord32(z.x) << 32) |
+              (unsigned long long)((ord32(__fadd_rn(z.y, 0.0f)) & ~1023u) | (unsigned)(1023 - tid));
+    }
+    // 1. each warp's k largest keys, in order (a popped key becomes zero)
+    {
+        unsigned long long mine = key;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const unsigned long long best = warp_max_key(mine);
+            if (lane == 0) wl[warp * kMaxTopK + j] = best;
+            if (mine == best) mine = 0ull;
+        }
+    }
+    __syncthreads();
+    // 2. warp 0 merges the sorted lists: lane l walks list l
+    if (warp == 0) {
+        int pos = 0;
+        unsigned long long head = lane < nw ? wl[lane * kMaxTopK] : 0ull;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const unsigned long long best = warp_max_key(head);
+            if (head == best) {
+                ++pos;
+                head = pos < k ? wl[lane * kMaxTopK + pos] : 0ull;
+            }
+            if (lane == 0) {
+                const int e = 1023 - (int)(best & 1023ull);
+                const float2 ze = w.z[e];
+                const float be = w.b[e];
+                w.sel[j] = e;
+                w.selz[j] = ze;
+                w.selb[j] = be;
+                lowb[j] = norm_pair(ze.x, __fsub_rd(ze.y, be));
+            }
+        }
+    }
+    __syncthreads();
+    // 3. Certified when every pick's lower bound lies above the upper bound of
+    // every expert ranked after it: each expert checks itself against the
+    // picks ranked before it (all k for an expert not picked), and the CTA
+    // takes the AND.
+    int good = 1;
+    if (tid < E) {
+        const float2 z = w.z[tid];
+        const float2 up = norm_pair(z.x, __fadd_ru(z.y, w.b[tid]));
+#pragma unroll 1
+        for (int j = 0; j < k && w.sel[j] != tid; ++j) good &= pair_gt(lowb[j], up) ? 1 : 0;
+    }
+    const int ok = __syncthreads_and(good);
+    if (warp == 0) {
+        if (ok) topk_weights(c, 0, w, ids_out, wts_out);
+        else topk_token(c, s, a, 0, reinterpret_cast<uint8_t*>(w.z64), rerank_flag, ids_out, wts_out);
+    }
+}
+
 // Top-k of token 0 by the first E threads of the CTA (E <= blockDim.x): thread
 // e builds expert e's key (the orderable 64-bit key of topk_token_fast: the
 // logit's high part, then its low part with 1023 - e in the low bits, so keys
@@ -677,6 +766,8 @@ __device__ __forceinline__ void topk_dispatch(const CacheDev& c, const Scratch& 
 // Plan of a decode call (T <= 32): the cache transaction, run by one CTA on
 // a copy of the pool's state held in shared memory.
 // ---------------------------------------------------------------------------
+constexpr int kVictimLists = 16;  // misses per call the fast victim search takes (more: one round per miss)
+
 struct PlanSmem {
     unsigned long long* lu;  // [K] last-use stamps of the pool
     int* kof;                // [K] keys of the pool's slots
@@ -694,6 +785,8 @@ struct PlanSmem {
     int* ids;                // [T*k] this call's picks
     unsigned long long* wmin;  // [32]
     int* wslot;              // [32]
+    unsigned long long* vkey;  // [32][kVictimLists]: each warp's smallest victim keys, in order
+    int* vslot;              // [32][kVictimLists]: their slots
     int* scal;               // [8]
     float* gl;               // [(E+1)*3] NVFP4 global scales of the layer (+ shared)
     size_t bytes;
@@ -723,6 +816,8 @@ __host__ __device__ inline PlanSmem plan_layout(uint8_t* base, int E, int K, int
     m.ids = (int*)take(sizeof(int) * n_ids);
     m.wmin = (unsigned long long*)take(sizeof(unsigned long long) * 32);
     m.wslot = (int*)take(sizeof(int) * 32);
+    m.vkey = (unsigned long long*)take(sizeof(unsigned long long) * 32 * kVictimLists);
+    m.vslot = (int*)take(sizeof(int) * 32 * kVictimLists);
     m.scal = (int*)take(sizeof(int) * 8);
     m.gl = (float*)take(sizeof(float) * (E + 1) * 3);
     m.bytes = off;
@@ -789,6 +884,76 @@ __device__ __forceinline__ void lfu_victim_keys(const CacheDev& c, const PlanSme
             u = (unsigned long long)(n < kLfuUseCap ? n : kLfuUseCap) + 1ull;
         }
         m.lu[i] = (u << 40) | (st & ((1ull << 40) - 1ull));
+    }
+    __syncthreads();
+}
+
+// The smallest of the lanes' 64-bit keys (the same pattern as warp_max_key).
+__device__ __forceinline__ unsigned long long warp_min_key(unsigned long long key) {
+    const unsigned hi = (unsigned)(key >> 32);
+    const unsigned mhi = __reduce_min_sync(0xffffffffu, hi);
+    const unsigned tied = __ballot_sync(0xffffffffu, hi == mhi);
+    if (__popc(tied) == 1) return __shfl_sync(0xffffffffu, key, __ffs(tied) - 1);
+    const unsigned lo = hi == mhi ? (unsigned)key : 0xffffffffu;
+    return ((unsigned long long)mhi << 32) | __reduce_min_sync(0xffffffffu, lo);
+}
+
+// The nmiss (<= kVictimLists) slots of the pool with the smallest keys, in
+// ascending order, into m.victims: the least recently used slots (keys are
+// the last-use stamps) or the LFU order (lfu_victim_keys). Keys are distinct,
+// except the ~0 of slots the call holds, which never rank among the nmiss
+// smallest. Thread t scans slots t, t + nthr, ... (at most 64 of them); each
+// warp takes its nmiss smallest keys by nmiss rounds of a warp-wide minimum,
+// where the winning lane then looks for its next smallest, into m.vkey /
+// m.vslot; warp 0 merges the warps' sorted lists the same way. The same
+// victims, in the same order, as nmiss rounds of a block-wide minimum. Every
+// thread of the block calls it.
+__device__ __forceinline__ void select_victims(const PlanSmem& m, int K, int nmiss) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    unsigned long long taken = 0ull;  // bit r: slot tid + r * nthr is already a victim
+    unsigned long long v = ~0ull;
+    int sl = -1;
+    auto next_smallest = [&]() {
+        v = ~0ull;
+        sl = -1;
+        int r = 0;
+        for (int i = tid; i < K; i += nthr, ++r)
+            if (!((taken >> r) & 1ull) && m.lu[i] < v) {
+                v = m.lu[i];
+                sl = i;
+            }
+    };
+    next_smallest();
+#pragma unroll 1
+    for (int j = 0; j < nmiss; ++j) {
+        const unsigned long long best = warp_min_key(v);
+        const unsigned win = __ballot_sync(0xffffffffu, v == best && sl >= 0);
+        const int wlane = win ? __ffs(win) - 1 : 0;
+        const int bsl = __shfl_sync(0xffffffffu, sl, wlane);
+        if (lane == 0) {
+            m.vkey[warp * kVictimLists + j] = win ? best : ~0ull;
+            m.vslot[warp * kVictimLists + j] = win ? bsl : -1;
+        }
+        if (win && lane == wlane) {
+            taken |= 1ull << ((bsl - tid) / nthr);
+            next_smallest();
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int pos = 0;
+        unsigned long long head = lane < nw ? m.vkey[lane * kVictimLists] : ~0ull;
+#pragma unroll 1
+        for (int j = 0; j < nmiss; ++j) {
+            const unsigned long long best = warp_min_key(head);
+            const unsigned win = __ballot_sync(0xffffffffu, head == best && lane < nw);
+            const int wlane = __ffs(win) - 1;
+            if (lane == wlane) {
+                m.victims[j] = m.vslot[lane * kVictimLists + pos];
+                ++pos;
+                head = pos < nmiss ? m.vkey[lane * kVictimLists + pos] : ~0ull;
+            }
+        }
     }
     __syncthreads();
 }
@@ -886,7 +1051,9 @@ static __device__ void plan_decode(const CacheDev& c, const Scratch& s, const Ro
     const int nmiss = nu - nh;
     if (c.lfu && nmiss > 0) lfu_victim_keys(c, m, clk);
     // 3. victims: the nmiss smallest stamps of the pool (LFU: keys), smallest first
-    if (nmiss > 0) {
+    if (nmiss > 0 && nmiss <= kVictimLists && K <= 64 * nthr) {
+        select_victims(m, K, nmiss);
+    } else if (nmiss > 0) {
         unsigned long long myv = ~0ull;
         int mys = -1;
         for (int i = tid; i < K; i += nthr)
@@ -990,6 +1157,18 @@ static __device__ void plan_decode(const CacheDev& c, const Scratch& s, const Ro
             if (!d.hit && c.fused_upload) {
                 d.src = (uint64_t)(c.store + ((size_t)layer * E + e) * c.slot_stride);
                 d.dst = slot_addr;
+                if (a.spec) {
+                    // predicted and prefetched one layer early: read the bank's copy
+                    const int half = layer & 1;
+                    const int* keys = c.bank_key + (size_t)half * c.bank_half;
+                    const int nb = c.bank_n[half];
+                    for (int j = 0; j < nb; ++j)
+                        if (keys[j] == layer * E + e) {
+                            d.src = (uint64_t)(c.bank + ((size_t)half * c.bank_half + j) * c.slot_stride);
+                            if (commit) atomicAdd(c.stats + 17, 1ull);
+                            break;
+                        }
+                }
             } else {
                 d.src = slot_addr;
                 d.dst = 0;
@@ -1128,7 +1307,9 @@ static __device__ __forceinline__ void plan_small(const CacheDev& c, const Scrat
     const int nmiss = nu - nh;
     if (c.lfu && nmiss > 0) lfu_victim_keys(c, m, clk);
     // 3. victims: the nmiss smallest stamps of the pool (LFU: keys), smallest first
-    if (nmiss > 0) {
+    if (nmiss > 0 && nmiss <= kVictimLists && K <= 64 * nthr) {
+        select_victims(m, K, nmiss);
+    } else if (nmiss > 0) {
         unsigned long long myv = ~0ull;
         int mys = -1;
         for (int i = tid; i < K; i += nthr)

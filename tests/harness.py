@@ -32,7 +32,7 @@ class Setup:
     """A GPU cache plus the workload's device inputs."""
 
     def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
-                 multi_wave=False, eviction="lru", norm_topk=True):
+                 multi_wave=False, eviction="lru", norm_topk=True, speculate=False):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -41,7 +41,8 @@ class Setup:
                               slots_per_layer=(K if K is not None else w.slots_per_layer),
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
-                              decode=decode, multi_wave=multi_wave, eviction=eviction, norm_topk=norm_topk)
+                              decode=decode, multi_wave=multi_wave, eviction=eviction, norm_topk=norm_topk,
+                              speculate=speculate)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):
@@ -58,6 +59,9 @@ class Setup:
         self.router_dev = [torch.from_numpy(r.view(np.int16)).to(dev) for r in self.router]
         self.bias_dev = None if self.bias is None else torch.from_numpy(self.bias).to(dev)
         self.dev = dev
+        if speculate:
+            for l in range(w.L):
+                self.cache.set_router(l, self.router_dev[l], self.bias_dev)
 
     def hiddens(self, layer, T, steps, rho=None):
         """[steps, T, H] bf16 bits: T independent AR(1) streams."""

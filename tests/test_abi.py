@@ -13,7 +13,7 @@ def test_library_exports_every_header_function():
     assert "moe_layer_forward" in names and "moe_cache_create" in names and "moe_cache_stats" in names
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
 
 
 def test_config_defaults():
@@ -24,6 +24,7 @@ def test_config_defaults():
     assert c.split_decode == 0  # automatic choice of the decode launch
     assert c.multi_wave == 0  # single-wave rule: over-capacity decode calls are refused
     assert c.eviction == 0  # least recently used
+    assert c.speculate == 0  # no speculative next-layer prefetch
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -38,6 +39,7 @@ def test_config_defaults():
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, max_cache_tokens=33), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, decode=3), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, eviction=2), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, speculate=True, upload_mode="memcpy"), pec.ERR_INVALID),
 ])
 def test_invalid_configurations_are_refused(kw, status):
     args = dict(kw)

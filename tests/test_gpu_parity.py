@@ -313,7 +313,8 @@ def test_exact_ties_one_token_on_both_decode_paths():
 
 @pytest.mark.parametrize("fmt,pool_mode,E,T", [
     ("q4_0", "per_layer", 64, 1), ("q4_0", "shared", 64, 3), ("fp8_b128", "per_layer", 40, 8),
-    ("nvfp4", "shared", 160, 2), ("bf16", "per_layer", 16, 4), ("nvfp4", "per_layer", 160, 4)])
+    ("nvfp4", "shared", 160, 2), ("bf16", "per_layer", 16, 4), ("nvfp4", "per_layer", 160, 4),
+    ("nvfp4", "shared", 512, 1), ("q4_0", "per_layer", 300, 1)])
 def test_one_kernel_and_three_kernel_decode_agree_bitwise(fmt, pool_mode, E, T):
     # The persistent one-kernel decode and the route / gate/up
     # / down kernels give the same bits: ids, slots, fills, outputs, final
