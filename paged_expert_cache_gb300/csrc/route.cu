@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(1024) k_plan_prefill(CacheDev c, Scratch s, Ro
 // ---------------------------------------------------------------------------
 constexpr int kPageinThreads = 1024;
 
-static size_t pagein_sort_len(int K) {
+__host__ __device__ inline size_t pagein_sort_len(int K) {
     size_t n = 1;
     while (n < (size_t)K) n <<= 1;
     return n;
