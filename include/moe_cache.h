@@ -113,6 +113,27 @@ typedef enum {
     MOE_EVICT_LFU = 1
 } moe_eviction_t;
 
+/* What a prefill call (T > max_cache_tokens) does to the cache. The pages
+ * differ:
+ *  MOE_PREFILL_READ_ONLY : resident experts are read in place, the others
+ *                          staged for the call only; the LRU order and the
+ *                          slots do not change [T4, "What the MoE Cache
+ *                          Actually Caches"].
+ *  MOE_PREFILL_PAGE_IN   : the prefill pages in every expert it routes to
+ *                          that is not resident, once [PAGED, "Why do short
+ *                          prompts get slower first tokens?"]: the decode
+ *                          transaction over all of the call's distinct
+ *                          experts, without the capacity rule (hits touched
+ *                          in first-occurrence order, then each miss in
+ *                          ascending order takes the least recently used
+ *                          slot; past K misses that is a slot the same call
+ *                          read or filled, and only the last expert placed in
+ *                          a slot stays). The records cross the host link
+ *                          once, through the staging arena, and those that
+ *                          stay are copied into their slots. Outputs are those
+ *                          of MOE_PREFILL_READ_ONLY. Needs MOE_EVICT_LRU. */
+typedef enum { MOE_PREFILL_READ_ONLY = 0, MOE_PREFILL_PAGE_IN = 1 } moe_prefill_mode_t;
+
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_experts;      /* E routed experts per layer, 1..1024 */
@@ -149,11 +170,12 @@ typedef struct {
                                  routing, the cache plan, the outputs, the stats and the trace are
                                  bitwise those of speculate = 0. Decode calls take the three-kernel
                                  path while it is on. */
+    int32_t prefill_mode;     /* moe_prefill_mode_t (default MOE_PREFILL_READ_ONLY) */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
  * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0,
- * MOE_EVICT_LRU, speculate 0; shape fields zero. */
+ * MOE_EVICT_LRU, speculate 0, MOE_PREFILL_READ_ONLY; shape fields zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {

@@ -22,6 +22,7 @@ POOL_MODES = {"per_layer": 0, "shared": 1}
 UPLOAD_MODES = {"pull": 0, "memcpy": 1}
 DECODE_MODES = {"auto": 0, "three_kernels": 1, "one_kernel": 2}
 EVICTIONS = {"lru": 0, "lfu": 1}
+PREFILL_MODES = {"read_only": 0, "page_in": 1}
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_OOM",
                 5: "MOE_ERR_STATE", 6: "MOE_ERR_TIMEOUT"}
 
@@ -33,7 +34,7 @@ class MoeConfig(ctypes.Structure):
                 ("format", i32), ("has_shared", i32), ("pool_mode", i32), ("slots_per_layer", i32),
                 ("upload_mode", i32), ("pool_bytes", dbl), ("norm_topk", i32), ("max_cache_tokens", i32),
                 ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32),
-                ("multi_wave", i32), ("eviction", i32), ("speculate", i32)]
+                ("multi_wave", i32), ("eviction", i32), ("speculate", i32), ("prefill_mode", i32)]
 
 
 class BucketStats(ctypes.Structure):
@@ -125,7 +126,8 @@ def _check(st, handle=None):
 
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
-                max_tokens=32, device=0, decode="auto", multi_wave=False, eviction="lru", speculate=False):
+                max_tokens=32, device=0, decode="auto", multi_wave=False, eviction="lru", speculate=False,
+                prefill="read_only"):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -144,6 +146,7 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.multi_wave = 1 if multi_wave else 0
     c.eviction = EVICTIONS[eviction] if isinstance(eviction, str) else int(eviction)
     c.speculate = 1 if speculate else 0
+    c.prefill_mode = PREFILL_MODES[prefill] if isinstance(prefill, str) else int(prefill)
     return c
 
 

@@ -178,6 +178,7 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->multi_wave = 0;
     cfg->eviction = MOE_EVICT_LRU;
     cfg->speculate = 0;
+    cfg->prefill_mode = MOE_PREFILL_READ_ONLY;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -213,6 +214,10 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     if (c.speculate != 0 && c.speculate != 1) return fail(nullptr, MOE_ERR_INVALID, "speculate must be 0 or 1");
     if (c.speculate && c.upload_mode != MOE_UPLOAD_PULL)
         return fail(nullptr, MOE_ERR_INVALID, "speculation needs MOE_UPLOAD_PULL");
+    if (c.prefill_mode != MOE_PREFILL_READ_ONLY && c.prefill_mode != MOE_PREFILL_PAGE_IN)
+        return fail(nullptr, MOE_ERR_INVALID, "unknown prefill_mode");
+    if (c.prefill_mode == MOE_PREFILL_PAGE_IN && c.eviction != MOE_EVICT_LRU)
+        return fail(nullptr, MOE_ERR_INVALID, "the page-in prefill needs LRU eviction");
     if (c.max_cache_tokens < 1 || c.max_cache_tokens > moe::kDecodeMaxTokens)
         return fail(nullptr, MOE_ERR_INVALID, "max_cache_tokens must be in 1..32");
     if (c.max_tokens < 1) return fail(nullptr, MOE_ERR_INVALID, "max_tokens must be >= 1");
@@ -297,6 +302,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(d.clock, (size_t)d.n_pools);
     DA(d.uses, (size_t)d.L * d.E);
     d.lfu = c.eviction == MOE_EVICT_LFU ? 1 : 0;
+    d.pagein = c.prefill_mode == MOE_PREFILL_PAGE_IN ? 1 : 0;
     DA(d.stats, 18);
     h->spec_w.assign(d.L, nullptr);
     h->spec_b.assign(d.L, nullptr);
@@ -606,6 +612,7 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         timed(h, 0, st, [&] { moe::launch_route(d, h->scr, a, units, st, false); });
         timed(h, 4, st, [&] { moe::launch_topk_prefill(d, h->scr, a, st); });
         timed(h, 5, st, [&] { moe::launch_plan_prefill(d, h->scr, a, h->G, st); });
+        if (d.pagein) timed(h, 5, st, [&] { moe::launch_pagein(d, h->scr, a, st); });
         const int groups = (std::min(T * d.k, d.E) + h->G - 1) / h->G;
         if (moe::gemm_supported(d)) {
             // tensor-core grouped GEMMs: resident units and the shared expert in
@@ -624,6 +631,9 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
                 CK(h, cudaEventRecord(h->ev_copy[g & 1], cs));
                 CK(h, cudaStreamWaitEvent(st, h->ev_copy[g & 1], 0));
                 timed(h, 2, st, [&] { moe::launch_gemm(d, h->scr, a.x, T, 2, g, h->G, h->G, st); });
+                // page-in: the group's records that stay resident go to their slots
+                // (after the resident units' GEMMs, before the arena half is restaged)
+                if (d.pagein) timed(h, 1, st, [&] { moe::launch_pagein_copy(d, h->scr, layer_id, g, h->G, st); });
                 CK(h, cudaEventRecord(h->ev_gemm[g & 1], st));
             }
             timed(h, 3, st, [&] { moe::launch_combine(d, h->scr, out, T, st); });
@@ -634,6 +644,7 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
                 timed(h, 1, st, [&] { moe::launch_copy(d, h->scr, g * h->G, h->G, bucket, st, false); });
                 timed(h, 2, st, [&] { moe::launch_gateup(d, h->scr, a.x, T, 2, g, h->G, h->G, st, false); });
                 timed(h, 3, st, [&] { moe::launch_down(d, h->scr, out, T, 2, g, h->G, h->G, bucket, st, false); });
+                if (d.pagein) timed(h, 1, st, [&] { moe::launch_pagein_copy(d, h->scr, layer_id, g, h->G, st); });
             }
         }
     }

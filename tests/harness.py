@@ -32,7 +32,7 @@ class Setup:
     """A GPU cache plus the workload's device inputs."""
 
     def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
-                 multi_wave=False, eviction="lru", norm_topk=True, speculate=False):
+                 multi_wave=False, eviction="lru", norm_topk=True, speculate=False, prefill="read_only"):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -42,7 +42,7 @@ class Setup:
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
                               decode=decode, multi_wave=multi_wave, eviction=eviction, norm_topk=norm_topk,
-                              speculate=speculate)
+                              speculate=speculate, prefill=prefill)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):
@@ -84,11 +84,11 @@ class Setup:
 class OracleRun:
     """The same calls through the oracle: routing, literal LRU, unpaged layer."""
 
-    def __init__(self, w, slot_bytes, K=None, policy="lru", norm=True):
+    def __init__(self, w, slot_bytes, K=None, policy="lru", norm=True, prefill="read_only"):
         self.w = w
         self.norm = norm
         self.K = pool_slots(w, slot_bytes, K)
-        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy)
+        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy, prefill=prefill)
         self._rec = {}
 
     def record(self, layer, e):

@@ -25,6 +25,7 @@ def test_config_defaults():
     assert c.multi_wave == 0  # single-wave rule: over-capacity decode calls are refused
     assert c.eviction == 0  # least recently used
     assert c.speculate == 0  # no speculative next-layer prefetch
+    assert c.prefill_mode == 0  # prefill reads the cache without changing it
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -40,6 +41,8 @@ def test_config_defaults():
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, decode=3), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, eviction=2), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, speculate=True, upload_mode="memcpy"), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, prefill=2), pec.ERR_INVALID),
+    (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, prefill="page_in", eviction="lfu"), pec.ERR_INVALID),
 ])
 def test_invalid_configurations_are_refused(kw, status):
     args = dict(kw)
