@@ -228,8 +228,10 @@ __host__ __device__ inline size_t pagein_sort_len(int K) {
     return n;
 }
 
+// keys [N] u64, L0 [K], first / use_slot / is_hit [E], hit-slot bits [K/32 + 1]:
+// at most 211 KB (K = 16384, E = 1024)
 static size_t pagein_smem(const CacheDev& c) {
-    return pagein_sort_len(c.K) * 8 + (size_t)c.K * 4 + (size_t)c.E * 12 + (size_t)c.K * 4;
+    return pagein_sort_len(c.K) * 8 + (size_t)c.K * 4 + (size_t)c.E * 12 + ((size_t)c.K / 32 + 1) * 4;
 }
 
 __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s, RouteArgs a) {
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
     int* first = L0 + K;                                                    // [E] first occurrence
     int* use_slot = first + E;                                              // [E] slot read from
     int* is_hit = use_slot + E;                                             // [E]
-    int* hit_slot = is_hit + E;                                             // [K] 1: a hit's slot
+    unsigned* hit_slot = reinterpret_cast<unsigned*>(is_hit + E);           // [K/32 + 1] bit: a hit's slot
     unsigned long long* g_lu = c.last_use + (size_t)pool * K;
     int* g_kof = c.key_of + (size_t)pool * K;
     int* g_smap = c.slot_map + (size_t)layer * E;
@@ -258,19 +260,20 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
         is_hit[e] = 0;
         use_slot[e] = -1;
     }
-    for (int i = tid; i < K; i += nthr) hit_slot[i] = 0;
+    for (int i = tid; i <= K / 32; i += nthr) hit_slot[i] = 0u;
     __syncthreads();
     for (int i = tid; i < n_ids; i += nthr) atomicMin(&first[s.ids[i]], i);
     for (int u = tid; u < nh; u += nthr) {
         const UnitDesc& d = s.units[u];
         is_hit[d.expert] = 1;
         use_slot[d.expert] = d.slot;
-        hit_slot[d.slot] = 1;
+        atomicOr(&hit_slot[d.slot >> 5], 1u << (d.slot & 31));
     }
     __syncthreads();
     // the untouched slots by ascending last-use stamp (stamps < 2^50, slots < 2^14)
     for (size_t i = tid; i < N; i += nthr)
-        key[i] = (i < (size_t)K && !hit_slot[i]) ? ((g_lu[i] << 14) | (unsigned long long)i) : ~0ull;
+        key[i] = (i < (size_t)K && !((hit_slot[i >> 5] >> (i & 31)) & 1u)) ? ((g_lu[i] << 14) | (unsigned long long)i)
+                                                                           : ~0ull;
     __syncthreads();
     for (size_t size = 2; size <= N; size <<= 1)
         for (size_t stride = size >> 1; stride > 0; stride >>= 1) {
