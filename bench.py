@@ -54,6 +54,9 @@ def parse():
                     help="speculative next-layer routing and prefetch (registers every layer's router)")
     ap.add_argument("--clock-ms", type=float, default=100.0,
                     help="interval of the clock and throttle-reason samples during the timed region")
+    ap.add_argument("--page-in", action="store_true",
+                    help="prefill calls page their missed experts into the pool (SGLang reading) instead of "
+                         "reading the cache without changing it")
     ap.add_argument("--prefill", action="store_true",
                     help="time prompt-sized calls (the prefill workload's prompt through each layer) instead of decode")
     return ap.parse_args()
@@ -433,10 +436,20 @@ def run_ours(args):
         else:
             step_layers()
 
-    for _ in range(args.warmup):
-        run_step()
-    torch.cuda.synchronize()
+    def reprime():
+        # the same history before each timed window: an empty cache, the
+        # priming steps and the warm-up steps through the graph
+        nonlocal cursor
+        cache.reset()
+        cursor = 0
+        for _ in range(PRIME):
+            next_inputs()
+            step_layers()
+        for _ in range(args.warmup):
+            run_step()
+        torch.cuda.synchronize()
 
+    reprime()
     s0 = cache.stats()
     clocks = ClockSampler(local, args.clock_ms)
     if dist:
@@ -464,20 +477,14 @@ def run_ours(args):
 
     # e2e: the same steps from the same cache state, with each step's inputs
     # copied in from pinned host memory and its outputs read back. The cache is
-    # reset and re-primed with the same priming and warm-up inputs (the cache is
-    # deterministic), so the window replays exactly the timed window's cache
-    # transactions, hits and misses, with the host copies added.
+    # reset and re-primed with the same priming and warm-up inputs as before the
+    # timed window (the cache is deterministic), so the window replays exactly
+    # the timed window's cache transactions, hits and misses, with the host
+    # copies added.
     e0_step = PRIME + args.warmup
     h_in = torch.from_numpy(hid[e0_step:e0_step + args.steps].view(np.int16)).pin_memory()
     h_out = torch.empty((w.L, T, w.H), dtype=torch.float32).pin_memory()
-    cache.reset()
-    cursor = 0
-    for _ in range(PRIME):
-        next_inputs()
-        step_layers()
-    for _ in range(args.warmup):
-        run_step()
-    torch.cuda.synchronize()
+    reprime()
     e_s0 = cache.stats()["buckets"][bk]
     if dist:
         dist.barrier()
@@ -700,7 +707,9 @@ def run_prefill(args):
     synth.build()
     import paged_expert_cache_gb300 as pec
     from synth.workloads import WORKLOADS, scaled
-    w = WORKLOADS[args.workload if args.workload != "qwen3_30b_a3b_q4_0" else "flash_next_prefill"]
+    w = WORKLOADS[args.workload]
+    if not w.prompt_T:
+        w = WORKLOADS["flash_next_prefill"]  # the workload that has a prompt
     if args.layers:
         w = scaled(w, L=args.layers)
     T = w.prompt_T
@@ -708,7 +717,7 @@ def run_prefill(args):
     torch.cuda.set_device(0)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,
-                          max_tokens=T, device=0)
+                          max_tokens=T, device=0, prefill="page_in" if args.page_in else "read_only")
     t_setup = time.perf_counter()
     cache = pec.MoECache(cfg)
     buf = None
@@ -727,15 +736,41 @@ def run_prefill(args):
     xs = [torch.from_numpy(synth.hidden_ar1(w.seed, l, 0, PRIME, w.H, w.rho).view(np.int16)).to(dev)
           for l in range(w.L)]
     dec_out = torch.empty((1, w.H), dtype=torch.float32, device=dev)
-    for s_ in range(PRIME):
-        for l in range(w.L):
-            cache.forward(xs[l][s_:s_ + 1], routers[l], l, dec_out, bias=bias, T=1)
-    torch.cuda.synchronize()
+
+    def prime_decode():
+        for s_ in range(PRIME):
+            for l in range(w.L):
+                cache.forward(xs[l][s_:s_ + 1], routers[l], l, dec_out, bias=bias, T=1)
+        torch.cuda.synchronize()
+
+    prime_decode()
     setup_s = time.perf_counter() - t_setup
 
     def prompt_pass():
         for l in range(w.L):
             cache.forward(prompts[l], routers[l], l, out, bias=bias, T=T)
+
+    # time to the first token's MoE work: the first prompt pass through every
+    # layer after a decode-primed cache (each repetition from a reset cache),
+    # which is when the page-in cost is paid [PAGED, "Why do short prompts get
+    # slower first tokens?"]
+    stream0 = torch.cuda.current_stream()
+    ttft = []
+    for _ in range(3):
+        cache.reset()
+        prime_decode()
+        b0 = cache.stats()["buckets"][2]
+        t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0e.record(stream0)
+        prompt_pass()
+        t1e.record(stream0)
+        torch.cuda.synchronize()
+        b1 = cache.stats()["buckets"][2]
+        ttft.append((t0e.elapsed_time(t1e), b1["misses"] - b0["misses"], b1["hits"] - b0["hits"]))
+    ttft.sort()
+    ttft_med = ttft[1]
+    cache.reset()
+    prime_decode()
 
     for _ in range(args.warmup):
         prompt_pass()
@@ -775,7 +810,12 @@ def run_prefill(args):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 tcgen05 products, fp32 accumulate in tensor memory", "data": "synthetic",
         "config": {"workload": w.name, "prompt_tokens": T, "layers": w.L, "experts": w.E, "top_k": w.k,
-                   "format": w.fmt, "prefill_group": 32, "priming_decode_steps": PRIME},
+                   "format": w.fmt, "prefill_group": 32, "priming_decode_steps": PRIME,
+                   "prefill_mode": "page_in" if args.page_in else "read_only"},
+        "first_prompt_pass": {"ms": ttft_med[0], "experts_staged": ttft_med[1], "experts_resident": ttft_med[2],
+                              "bytes_over_link": ttft_med[1] * cache.info()["slot_bytes"],
+                              "note": "MoE layers only: the prompt through all layers once, from a cache primed by "
+                                      "decode steps (median of 3, each from a reset cache)"},
         "per_layer_call_us": ms * 1e3 / (args.steps * calls),
         "resident_experts_per_call": hits / max(1, args.steps * calls),
         "staged_experts_per_call": staged / max(1, args.steps * calls),

@@ -78,6 +78,8 @@ def lib():
         L.orc_wave_split.argtypes = [i32, i32, i32, vp, vp]
         L.orc_cache_set_policy.argtypes = [vp, i32]
         L.orc_cache_set_prefill_mode.argtypes = [vp, i32]
+        L.orc_cache_set_adaptive.argtypes = [vp, i32, i32, i32, i32]
+        L.orc_cache_pool_slots.argtypes = [vp, i32]
         _lib = L
     return _lib
 
@@ -200,7 +202,7 @@ class Cache:
     """The literal LRU list (moe_oracle.c), one instance per simulated cache."""
 
     def __init__(self, L, E, pool_mode, slots_per_pool, slot_bytes=0.0, max_cache_tokens=32, policy="lru",
-                 prefill="read_only"):
+                 prefill="read_only", adaptive=None):
         self.L, self.E = L, E
         self.h = lib().orc_cache_create(L, E, POOL[pool_mode] if isinstance(pool_mode, str) else pool_mode,
                                         slots_per_pool, float(slot_bytes), max_cache_tokens)
@@ -210,8 +212,15 @@ class Cache:
             raise ValueError("invalid eviction policy")
         if lib().orc_cache_set_prefill_mode(self.h, PREFILL.get(prefill, -1)) != OK:
             raise ValueError("invalid prefill mode")
+        if adaptive is not None:  # (period, step, kmin, kmax)
+            if lib().orc_cache_set_adaptive(self.h, *[int(v) for v in adaptive]) != OK:
+                raise ValueError("invalid adaptive capacity")
         self.n_pools = lib().orc_cache_num_pools(self.h)
         self.K = lib().orc_cache_slots(self.h)
+
+    def pool_slots(self):
+        """Slots each pool holds now (the configured K unless capacity adapts)."""
+        return [int(lib().orc_cache_pool_slots(self.h, p)) for p in range(self.n_pools)]
 
     def __del__(self):
         h = getattr(self, "h", None)

@@ -383,9 +383,20 @@ struct orc_cache {
     char* inuse;     /* [K] scratch: slots the current call holds (LFU) */
     int prefill_mode;   /* ORC_PREFILL_READ_ONLY or ORC_PREFILL_PAGE_IN */
     int32_t* use_slot;  /* [E] scratch: the slot an expert is read from in the current call */
+    /* adaptive per-layer capacity (per-layer pools): each pool's array has K
+     * places, of which Kp[p] are its slots (active[p*K + s]); K0 slots each at
+     * the start; every period*L decode calls capacity moves (see
+     * orc_cache_set_adaptive) */
+    int K0;
+    int32_t* Kp;          /* [n_pools] */
+    char* active;         /* [n_pools*K] */
+    int adapt_period, adapt_step, adapt_kmin;
+    uint64_t decode_calls;
+    uint64_t* win;        /* [L][2] hits, misses of decode calls since the last move */
 };
 
-/* Initial list: every slot empty, ordered 0..K-1 with slot 0 at the head. */
+/* Initial list: every slot empty, ordered 0..K0-1 with slot 0 at the head
+ * (places K0..K-1 of an adaptive pool hold no slot yet). */
 void orc_cache_reset(orc_cache* c) {
     int p, s;
     for (s = 0; s < c->L * c->E; ++s) c->slot_map[s] = -1;
@@ -394,14 +405,18 @@ void orc_cache_reset(orc_cache* c) {
         int32_t* nx = c->next + (size_t)p * c->K;
         for (s = 0; s < c->K; ++s) {
             c->key_of[(size_t)p * c->K + s] = -1;
-            pv[s] = s - 1;
-            nx[s] = (s + 1 < c->K) ? s + 1 : -1;
+            c->active[(size_t)p * c->K + s] = s < c->K0;
+            pv[s] = s < c->K0 ? s - 1 : -1;
+            nx[s] = (s + 1 < c->K0) ? s + 1 : -1;
         }
         c->head[p] = 0;
-        c->tail[p] = c->K - 1;
+        c->tail[p] = c->K0 - 1;
+        c->Kp[p] = c->K0;
     }
     memset(c->stats, 0, sizeof(c->stats));
     memset(c->uses, 0, sizeof(uint64_t) * (size_t)c->L * c->E);
+    memset(c->win, 0, sizeof(uint64_t) * 2 * (size_t)c->L);
+    c->decode_calls = 0;
 }
 
 orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, double slot_bytes,
@@ -429,6 +444,10 @@ orc_cache* orc_cache_create(int L, int E, int pool_mode, int slots_per_pool, dou
     c->uses = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)L * E);
     c->inuse = (char*)malloc((size_t)c->K);
     c->use_slot = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+    c->K0 = c->K;
+    c->Kp = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->n_pools);
+    c->active = (char*)malloc((size_t)c->n_pools * c->K);
+    c->win = (uint64_t*)malloc(sizeof(uint64_t) * 2 * (size_t)L);
     c->policy = ORC_POLICY_LRU;
     c->prefill_mode = ORC_PREFILL_READ_ONLY;
     orc_cache_reset(c);
@@ -476,9 +495,103 @@ int orc_cache_set_prefill_mode(orc_cache* c, int mode) {
     return ORC_OK;
 }
 
+/* Adaptive per-layer capacity [FP4LOCAL, "Decode"]: "some capacity is moved
+ * from layers with high hit rates to layers with low hit rates" as decoding
+ * progresses, with the same total. The page prints no rule; reading taken:
+ * per-layer pools; every period * L decode calls (each wave a call; prefill
+ * calls do not count), the layer whose decode calls since the last move had
+ * the highest hit rate (hits / (hits + misses)) gives `step` slots, one at a
+ * time, to the layer with the lowest, lower layer first on ties (rates are
+ * compared exactly, h1 (h2 + m2) against h2 (h1 + m1)), layers without a
+ * decode call in the window taking no part; the giver keeps at least kmin
+ * slots and the taker at most kmax. A moved slot is the giver's least
+ * recently used one, its expert evicted; it becomes the taker's empty least
+ * recently used slot, at the lowest place of its array that holds no slot.
+ * No move when the two rates are equal. The window then restarts. */
+int orc_cache_set_adaptive(orc_cache* c, int period, int step, int kmin, int kmax) {
+    int32_t *ko, *pv, *nx;
+    char *in, *ac;
+    if (!c || c->mode != ORC_POOL_PER_LAYER || period < 1 || step < 1 || kmin < 1 || kmin > c->K0 ||
+        kmax < c->K0)
+        return ORC_ERR_INVALID;
+    ko = (int32_t*)realloc(c->key_of, sizeof(int32_t) * (size_t)c->n_pools * kmax);
+    pv = (int32_t*)realloc(c->prev, sizeof(int32_t) * (size_t)c->n_pools * kmax);
+    nx = (int32_t*)realloc(c->next, sizeof(int32_t) * (size_t)c->n_pools * kmax);
+    in = (char*)realloc(c->inuse, (size_t)kmax);
+    ac = (char*)realloc(c->active, (size_t)c->n_pools * kmax);
+    if (!ko || !pv || !nx || !in || !ac) return ORC_ERR_INVALID;
+    c->key_of = ko;
+    c->prev = pv;
+    c->next = nx;
+    c->inuse = in;
+    c->active = ac;
+    c->K = kmax;
+    c->adapt_period = period;
+    c->adapt_step = step;
+    c->adapt_kmin = kmin;
+    orc_cache_reset(c);
+    return ORC_OK;
+}
+
+/* One slot from pool d to pool r (adaptive capacity). */
+static void adapt_move(orc_cache* c, int d, int r) {
+    int32_t* pv = c->prev + (size_t)d * c->K;
+    int32_t* nx = c->next + (size_t)d * c->K;
+    const int32_t s = c->head[d];
+    const int32_t key = c->key_of[(size_t)d * c->K + s];
+    int32_t t;
+    if (key >= 0) c->slot_map[key] = -1;
+    c->key_of[(size_t)d * c->K + s] = -1;
+    c->head[d] = nx[s];
+    if (nx[s] >= 0) pv[nx[s]] = -1;
+    else c->tail[d] = -1;
+    c->active[(size_t)d * c->K + s] = 0;
+    c->Kp[d]--;
+    for (t = 0; c->active[(size_t)r * c->K + t]; ++t) {
+    }
+    pv = c->prev + (size_t)r * c->K;
+    nx = c->next + (size_t)r * c->K;
+    c->active[(size_t)r * c->K + t] = 1;
+    c->key_of[(size_t)r * c->K + t] = -1;
+    pv[t] = -1;
+    nx[t] = c->head[r];
+    if (c->head[r] >= 0) pv[c->head[r]] = t;
+    else c->tail[r] = t;
+    c->head[r] = t;
+    c->Kp[r]++;
+}
+
+static void adapt_after_call(orc_cache* c) {
+    int l, d = -1, r = -1, i;
+    if (!c->adapt_period) return;
+    c->decode_calls++;
+    if (c->decode_calls % ((uint64_t)c->adapt_period * c->L) != 0) return;
+    for (l = 0; l < c->L; ++l) {
+        const uint64_t h = c->win[2 * l], m = c->win[2 * l + 1];
+        if (h + m == 0) continue;
+        if (c->Kp[l] - c->adapt_step >= c->adapt_kmin &&
+            (d < 0 || h * (c->win[2 * d] + c->win[2 * d + 1]) > c->win[2 * d] * (h + m)))
+            d = l;
+        if (c->Kp[l] + c->adapt_step <= c->K &&
+            (r < 0 || h * (c->win[2 * r] + c->win[2 * r + 1]) < c->win[2 * r] * (h + m)))
+            r = l;
+    }
+    if (d >= 0 && r >= 0 && d != r &&
+        c->win[2 * d] * (c->win[2 * r] + c->win[2 * r + 1]) > c->win[2 * r] * (c->win[2 * d] + c->win[2 * d + 1]))
+        for (i = 0; i < c->adapt_step; ++i) adapt_move(c, d, r);
+    memset(c->win, 0, sizeof(uint64_t) * 2 * (size_t)c->L);
+}
+
+int orc_cache_pool_slots(const orc_cache* c, int pool) {
+    return (!c || pool < 0 || pool >= c->n_pools) ? -1 : c->Kp[pool];
+}
+
 void orc_cache_destroy(orc_cache* c) {
     if (!c) return;
     free(c->use_slot);
+    free(c->Kp);
+    free(c->active);
+    free(c->win);
     free(c->slot_map);
     free(c->key_of);
     free(c->prev);
@@ -614,7 +727,7 @@ int orc_cache_plan(orc_cache* c, int layer, const int32_t* ids, int n_ids, int T
         return ORC_OK;
     }
 
-    if (nu > c->K) return ORC_ERR_CAPACITY;
+    if (nu > c->Kp[p]) return ORC_ERR_CAPACITY;
 
     if (c->policy == ORC_POLICY_LFU) {
         memset(c->inuse, 0, (size_t)c->K);
@@ -674,6 +787,9 @@ int orc_cache_plan(orc_cache* c, int layer, const int32_t* ids, int n_ids, int T
     *n_fill = nf;
     *n_hit = nh;
     *n_uniq = nu;
+    c->win[2 * layer] += (uint64_t)nh;
+    c->win[2 * layer + 1] += (uint64_t)nf;
+    adapt_after_call(c);
     return ORC_OK;
 }
 

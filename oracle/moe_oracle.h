@@ -124,6 +124,16 @@ int orc_cache_set_policy(orc_cache* c, int policy);
 /* Prefill mode (ORC_PREFILL_READ_ONLY, the default, or ORC_PREFILL_PAGE_IN,
  * which needs LRU). ORC_ERR_INVALID otherwise. */
 int orc_cache_set_prefill_mode(orc_cache* c, int mode);
+/* Adaptive per-layer capacity (per-layer pools): every period * L decode
+ * calls, `step` slots move, one at a time, from the layer with the highest
+ * hit rate since the last move to the one with the lowest, within
+ * [kmin, kmax] slots per layer; a moved slot leaves as its giver's least
+ * recently used (expert evicted) and arrives as the taker's empty least
+ * recently used, at the lowest free place of its array of kmax places.
+ * Resets the cache. ORC_ERR_INVALID for a shared pool or bad bounds. */
+int orc_cache_set_adaptive(orc_cache* c, int period, int step, int kmin, int kmax);
+/* Slots pool `pool` holds now. */
+int orc_cache_pool_slots(const orc_cache* c, int pool);
 /* The waves of a decode step of T tokens on a pool of K slots: successive
  * groups of K // k tokens; returns their number (0 if K < k). */
 int orc_wave_split(int T, int k, int K, int32_t* start, int32_t* count);
