@@ -171,11 +171,31 @@ typedef struct {
                                  bitwise those of speculate = 0. Decode calls take the three-kernel
                                  path while it is on. */
     int32_t prefill_mode;     /* moe_prefill_mode_t (default MOE_PREFILL_READ_ONLY) */
+    int32_t adapt_period;     /* 0 (default): every layer keeps slots_per_layer slots. > 0 (per-layer
+                                 pools): adaptive per-layer capacity [FP4LOCAL, "Decode": capacity
+                                 moves from layers with high hit rates to layers with low hit
+                                 rates, same total]. Every adapt_period * L decode calls (each wave
+                                 a call; prefill calls do not count), adapt_step slots move, one at
+                                 a time, from the layer whose decode calls since the last move had
+                                 the highest hit rate to the one with the lowest (exact comparison,
+                                 the lower layer first on ties; layers without a decode call in the
+                                 window take no part; no move on equal rates), within
+                                 [adapt_min_slots, adapt_max_slots] slots per layer. A moved slot
+                                 leaves as the giver's least recently used (its expert evicted) and
+                                 arrives as the taker's empty least recently used slot, at the
+                                 lowest place of the taker's array that holds no slot. Each layer's
+                                 array has adapt_max_slots places in device memory (the logical
+                                 total stays L * slots_per_layer); the single-wave rule uses
+                                 adapt_min_slots. */
+    int32_t adapt_step;       /* slots per move (0: 1) */
+    int32_t adapt_min_slots;  /* fewest slots a layer keeps (0: max(top_k, slots_per_layer / 2)) */
+    int32_t adapt_max_slots;  /* most slots a layer holds (0: 2 * slots_per_layer - adapt_min_slots) */
 } moe_config_t;
 
 /* Fills cfg with defaults: norm_topk 1, max_cache_tokens 32, prefill_group 32,
  * max_tokens 32, upload PULL, per-layer pools, MOE_DECODE_AUTO, multi_wave 0,
- * MOE_EVICT_LRU, speculate 0, MOE_PREFILL_READ_ONLY; shape fields zero. */
+ * MOE_EVICT_LRU, speculate 0, MOE_PREFILL_READ_ONLY, adapt_period 0; shape
+ * fields zero. */
 void moe_config_default(moe_config_t* cfg);
 
 typedef struct {
@@ -305,6 +325,11 @@ moe_status_t moe_cache_trace_enable(moe_cache_t* h, int32_t capacity_calls);
  * is too small for the records held. */
 moe_status_t moe_cache_trace_read(moe_cache_t* h, int32_t* buf, int64_t buf_words, int64_t* n_words,
                                   int32_t* n_records);
+
+/* Synchronises and copies the number of slots each pool holds now into
+ * sizes [pools] (host int32): slots_per_layer (or the shared pool's slots)
+ * unless the per-layer capacity adapts. */
+moe_status_t moe_cache_pool_slots(moe_cache_t* h, int32_t* sizes);
 
 /* Synchronises and copies the cache state: slot_map [L x E] (slot or -1),
  * key_of [pools x K] (layer*E + expert or -1), order [pools x K] (slots from

@@ -34,7 +34,8 @@ class MoeConfig(ctypes.Structure):
                 ("format", i32), ("has_shared", i32), ("pool_mode", i32), ("slots_per_layer", i32),
                 ("upload_mode", i32), ("pool_bytes", dbl), ("norm_topk", i32), ("max_cache_tokens", i32),
                 ("prefill_group", i32), ("max_tokens", i32), ("device", i32), ("split_decode", i32),
-                ("multi_wave", i32), ("eviction", i32), ("speculate", i32), ("prefill_mode", i32)]
+                ("multi_wave", i32), ("eviction", i32), ("speculate", i32), ("prefill_mode", i32),
+                ("adapt_period", i32), ("adapt_step", i32), ("adapt_min_slots", i32), ("adapt_max_slots", i32)]
 
 
 class BucketStats(ctypes.Structure):
@@ -94,6 +95,7 @@ def load():
         "moe_cache_profile_read": (i32, [vp, P(MoeProfile)]),
         "moe_route_topk_noalloc": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
         "moe_cache_set_router": (i32, [vp, i32, vp, vp]),
+        "moe_cache_pool_slots": (i32, [vp, vp]),
         "moe_cache_reset": (i32, [vp]),
         "moe_cache_destroy": (i32, [vp]),
     }
@@ -127,7 +129,7 @@ def _check(st, handle=None):
 def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_layer=0, pool_bytes=0.0,
                 has_shared=False, upload_mode="pull", norm_topk=True, max_cache_tokens=32, prefill_group=32,
                 max_tokens=32, device=0, decode="auto", multi_wave=False, eviction="lru", speculate=False,
-                prefill="read_only"):
+                prefill="read_only", adapt=None):
     c = MoeConfig()
     load().moe_config_default(ctypes.byref(c))
     c.num_layers, c.num_experts, c.top_k, c.hidden, c.inter = L, E, k, H, I
@@ -147,6 +149,8 @@ def make_config(L, E, k, H, I, fmt="bf16", pool_mode="per_layer", slots_per_laye
     c.eviction = EVICTIONS[eviction] if isinstance(eviction, str) else int(eviction)
     c.speculate = 1 if speculate else 0
     c.prefill_mode = PREFILL_MODES[prefill] if isinstance(prefill, str) else int(prefill)
+    if adapt is not None:  # (period, step, min slots, max slots); 0 takes the default
+        c.adapt_period, c.adapt_step, c.adapt_min_slots, c.adapt_max_slots = (int(v) for v in adapt)
     return c
 
 
@@ -283,6 +287,13 @@ class MoECache:
         device fp32 [E] or None) for speculative next-layer routing; the
         tensors must stay alive and unchanged while registered."""
         _check(load().moe_cache_set_router(self.h, layer, _ptr(router_w), _ptr(bias)), self.h)
+
+    def pool_slots(self):
+        """moe_cache_pool_slots: the slots each pool holds now."""
+        n = self.info()["num_pools"]
+        out = np.empty(n, dtype=np.int32)
+        _check(load().moe_cache_pool_slots(self.h, out.ctypes.data), self.h)
+        return out.tolist()
 
     def stats(self):
         s = MoeStats()

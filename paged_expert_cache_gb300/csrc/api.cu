@@ -138,6 +138,22 @@ moe_status_t init_tables(moe_cache_t* h) {
     std::vector<unsigned long long> lu((size_t)d.n_pools * d.K), clk(d.n_pools, (unsigned long long)d.K);
     for (int p = 0; p < d.n_pools; ++p)
         for (int s = 0; s < d.K; ++s) lu[(size_t)p * d.K + s] = (unsigned long long)s;
+    if (d.adapt_period) {
+        // places 0..K0-1 hold the slots at the start; the stamps start at 2^32
+        // so slots that arrive later can be stamped below all of them
+        const unsigned long long base = 1ull << 32;
+        const int K0 = h->cfg.slots_per_layer;
+        for (int p = 0; p < d.n_pools; ++p) {
+            for (int s = 0; s < d.K; ++s) lu[(size_t)p * d.K + s] = s < K0 ? base + s : ~0ull;
+            clk[p] = base + K0;
+        }
+        std::vector<int> pk(d.n_pools, K0);
+        std::vector<unsigned long long> fl(d.n_pools, base - 1);
+        CK(h, cudaMemcpy(d.pool_K, pk.data(), pk.size() * sizeof(int), cudaMemcpyHostToDevice));
+        CK(h, cudaMemcpy(d.floor_stamp, fl.data(), fl.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
+        CK(h, cudaMemset(d.win, 0, 2 * (size_t)d.L * sizeof(unsigned)));
+        CK(h, cudaMemset(d.adapt_calls, 0, sizeof(unsigned long long)));
+    }
     CK(h, cudaMemcpy(d.slot_map, sm.data(), sm.size() * sizeof(int), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.key_of, ko.data(), ko.size() * sizeof(int), cudaMemcpyHostToDevice));
     CK(h, cudaMemcpy(d.last_use, lu.data(), lu.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
@@ -179,6 +195,10 @@ void moe_config_default(moe_config_t* cfg) {
     cfg->eviction = MOE_EVICT_LRU;
     cfg->speculate = 0;
     cfg->prefill_mode = MOE_PREFILL_READ_ONLY;
+    cfg->adapt_period = 0;
+    cfg->adapt_step = 0;
+    cfg->adapt_min_slots = 0;
+    cfg->adapt_max_slots = 0;
 }
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -218,13 +238,27 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         return fail(nullptr, MOE_ERR_INVALID, "unknown prefill_mode");
     if (c.prefill_mode == MOE_PREFILL_PAGE_IN && c.eviction != MOE_EVICT_LRU)
         return fail(nullptr, MOE_ERR_INVALID, "the page-in prefill needs LRU eviction");
+    moe_config_t cc = c;  // with the adaptive capacity's defaults filled in
+    if (cc.adapt_period < 0) return fail(nullptr, MOE_ERR_INVALID, "adapt_period must be >= 0");
+    if (cc.adapt_period > 0) {
+        if (cc.pool_mode != MOE_POOL_PER_LAYER)
+            return fail(nullptr, MOE_ERR_INVALID, "adaptive capacity needs per-layer pools");
+        if (cc.adapt_step == 0) cc.adapt_step = 1;
+        if (cc.adapt_min_slots == 0) cc.adapt_min_slots = std::max(cc.top_k, cc.slots_per_layer / 2);
+        if (cc.adapt_max_slots == 0) cc.adapt_max_slots = 2 * cc.slots_per_layer - cc.adapt_min_slots;
+        if (cc.adapt_step < 1 || cc.adapt_min_slots < cc.top_k || cc.adapt_min_slots > cc.slots_per_layer ||
+            cc.adapt_max_slots < cc.slots_per_layer || cc.adapt_max_slots > 16384)
+            return fail(nullptr, MOE_ERR_INVALID,
+                        "adaptive capacity needs top_k <= adapt_min_slots <= slots_per_layer <= adapt_max_slots "
+                        "<= 16384 and adapt_step >= 1");
+    }
     if (c.max_cache_tokens < 1 || c.max_cache_tokens > moe::kDecodeMaxTokens)
         return fail(nullptr, MOE_ERR_INVALID, "max_cache_tokens must be in 1..32");
     if (c.max_tokens < 1) return fail(nullptr, MOE_ERR_INVALID, "max_tokens must be >= 1");
     if (c.prefill_group < 1 || c.prefill_group > 1024) return fail(nullptr, MOE_ERR_INVALID, "prefill_group in 1..1024");
 
     moe_cache_t* h = new moe_cache();
-    h->cfg = c;
+    h->cfg = cc;
     moe::CacheDev& d = h->dev;
     d.L = c.num_layers; d.E = c.num_experts; d.k = c.top_k; d.H = c.hidden; d.I = c.inter;
     d.fmt = c.format; d.has_shared = c.has_shared ? 1 : 0; d.norm_topk = c.norm_topk ? 1 : 0;
@@ -238,13 +272,16 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     d.slot_stride = h->slot_stride;
     if (c.pool_mode == MOE_POOL_PER_LAYER) {
         d.n_pools = d.L;
-        d.K = c.slots_per_layer;
+        d.K = cc.adapt_period ? cc.adapt_max_slots : c.slots_per_layer;
+        d.adapt_period = cc.adapt_period;
+        d.adapt_step = cc.adapt_step;
+        d.adapt_kmin = cc.adapt_min_slots;
     } else {
         d.n_pools = 1;
         double k = c.pool_bytes > 0 ? floor(c.pool_bytes / (double)h->slot_bytes) : 0.0;
         d.K = k > 1e9 ? 1000000000 : (int)k;
     }
-    if (d.K < d.k) {
+    if ((c.pool_mode == MOE_POOL_PER_LAYER ? c.slots_per_layer : d.K) < d.k) {
         char msg[160];
         snprintf(msg, sizeof msg, "pool has %d slots, fewer than top_k = %d", d.K, d.k);
         delete h;
@@ -304,6 +341,12 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     d.lfu = c.eviction == MOE_EVICT_LFU ? 1 : 0;
     d.pagein = c.prefill_mode == MOE_PREFILL_PAGE_IN ? 1 : 0;
     DA(d.stats, 18);
+    if (d.adapt_period) {
+        DA(d.pool_K, (size_t)d.n_pools);
+        DA(d.win, 2 * (size_t)d.L);
+        DA(d.adapt_calls, 1);
+        DA(d.floor_stamp, (size_t)d.n_pools);
+    }
     h->spec_w.assign(d.L, nullptr);
     h->spec_b.assign(d.L, nullptr);
     if (c.speculate) {
@@ -469,13 +512,15 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
         return fail(h, MOE_ERR_STATE, "experts not loaded");
     cudaStream_t st = (cudaStream_t)stream;
     const bool decode = T <= h->cfg.max_cache_tokens;
-    if (decode && (int64_t)T * d.k > d.K) {
+    // the single-wave rule: a pool whose capacity adapts is held to its minimum
+    const int cap = d.adapt_period ? d.adapt_kmin : d.K;
+    if (decode && (int64_t)T * d.k > cap) {
         if (!h->cfg.multi_wave)
             return fail(h, MOE_ERR_CAPACITY, "tokens * top_k exceeds the slots of this layer's pool");
         // Several waves, each within the single-wave rule: floor(K / k) tokens
         // per wave (at least one, since create requires K >= k), in token
         // order, each its own cache transaction.
-        const int per_wave = d.K / d.k;
+        const int per_wave = cap / d.k;
         for (int t0 = 0; t0 < T; t0 += per_wave) {
             const int tw = std::min(per_wave, T - t0);
             const moe_status_t r = moe_layer_forward(h, (const uint16_t*)hidden + (size_t)t0 * d.H, tw, router_w,
@@ -497,7 +542,7 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     // call. When the call just before this one on the handle was another
     // layer's, that write belongs to a grid at least two back in stream order,
     // which has completed by the time this call's kernel can start.
-    a.early = (d.pool_mode == 0 && h->last_layer >= 0 && h->last_layer != layer_id) ? 1 : 0;
+    a.early = (d.pool_mode == 0 && !d.adapt_period && h->last_layer >= 0 && h->last_layer != layer_id) ? 1 : 0;
     h->last_layer = layer_id;
     const int units = std::min(T * d.k, d.E) + d.has_shared;
     // Speculation: the side stream's prefetch for layer spec_pending. Its bank
@@ -648,8 +693,20 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
             }
         }
     }
+    if (decode && d.adapt_period) moe::launch_adapt(d, st);  // counts the call; moves capacity on its period
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_cache_pool_slots(moe_cache_t* h, int32_t* sizes) {
+    if (!h || !sizes) return fail(h, MOE_ERR_INVALID, "NULL argument");
+    const moe::CacheDev& d = h->dev;
+    CK(h, cudaSetDevice(h->cfg.device));
+    CK(h, cudaDeviceSynchronize());
+    if (d.pool_K) CK(h, cudaMemcpy(sizes, d.pool_K, sizeof(int) * (size_t)d.n_pools, cudaMemcpyDeviceToHost));
+    else
+        for (int p = 0; p < d.n_pools; ++p) sizes[p] = d.K;
     return MOE_OK;
 }
 
@@ -766,10 +823,13 @@ moe_status_t moe_cache_get_state(moe_cache_t* h, int32_t* slot_map, int32_t* key
         std::vector<unsigned long long> lu((size_t)d.n_pools * d.K);
         CK(h, cudaMemcpy(lu.data(), d.last_use, lu.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
         for (int p = 0; p < d.n_pools; ++p) {
-            std::vector<int> idx(d.K);
-            for (int s = 0; s < d.K; ++s) idx[s] = s;
+            // the places that hold a slot (stamp not ~0), least recent first
             const unsigned long long* v = lu.data() + (size_t)p * d.K;
+            std::vector<int> idx;
+            for (int s = 0; s < d.K; ++s)
+                if (v[s] != ~0ull) idx.push_back(s);
             std::sort(idx.begin(), idx.end(), [&](int a, int b) { return v[a] < v[b]; });
+            idx.resize(d.K, -1);
             memcpy(order + (size_t)p * d.K, idx.data(), sizeof(int) * d.K);
         }
     }

@@ -51,7 +51,8 @@ struct Plan {
     int n_units;  // compute units: n_uniq (+1 shared expert)
     int status;   // 0 ok; 2 capacity exceeded (nothing changed)
     int reranked; // 1 if the fp64 re-rank decided the top-k of some token
-    int pad[2];
+    int pool_slots;  // page-in prefill: slots the layer's pool held during the call
+    int pad;
 };
 
 // One compute unit of a call (a distinct routed expert, or the shared
@@ -128,6 +129,13 @@ struct CacheDev {
     int* bank_n;                   // [2]: bank slots filled in each half
     int bank_half;                 // bank slots per half (layer parity)
     int pagein;                    // 1: prefill calls page their missed experts into the pool (LRU)
+    // adaptive per-layer capacity (null / 0 when off): a place of a pool's
+    // array holds a slot while its stamp is not ~0
+    int adapt_period, adapt_step, adapt_kmin;
+    int* pool_K;                   // [n_pools] slots each pool holds
+    unsigned* win;                 // [L][2] hits, misses of decode calls since the last move
+    unsigned long long* adapt_calls;  // decode calls so far
+    unsigned long long* floor_stamp;  // [n_pools] the next stamp of an arriving slot (decreasing)
     int* trace;                    // ring of records, or null
     unsigned long long* trace_count;
     int trace_cap, trace_stride;
@@ -296,6 +304,9 @@ void launch_plan_prefill(const CacheDev& c, const Scratch& s, const RouteArgs& a
 // into their slots, after the GEMMs of their staging group.
 void launch_pagein(const CacheDev& c, const Scratch& s, const RouteArgs& a, cudaStream_t st);
 void launch_pagein_copy(const CacheDev& c, const Scratch& s, int layer, int group, int G, cudaStream_t st);
+// Adaptive per-layer capacity: after a decode call, counts it and, every
+// adapt_period * L calls, moves slots between the layers' pools.
+void launch_adapt(const CacheDev& c, cudaStream_t st);
 void launch_copy(const CacheDev& c, const Scratch& s, int first, int count, int bucket, cudaStream_t st,
                  bool beside_compute);
 void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T, int kind, int group, int G,

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
     const int pool = c.pool_mode ? 0 : layer;
     const int n_ids = a.T * k;
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const Plan* pl = s.plan;
+    Plan* pl = s.plan;
     const int nu = pl->n_uniq, nh = pl->n_hit, nm = nu - nh;
     const size_t N = pagein_sort_len(K);
     unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);  // [N] sort keys
@@ -254,7 +254,11 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
     int* g_kof = c.key_of + (size_t)pool * K;
     int* g_smap = c.slot_map + (size_t)layer * E;
     __shared__ unsigned long long clk;
-    if (tid == 0) clk = c.clock[pool];
+    __shared__ int Kl;  // slots the pool holds (places whose stamp is not ~0)
+    if (tid == 0) {
+        clk = c.clock[pool];
+        Kl = 0;
+    }
     for (int e = tid; e < E; e += nthr) {
         first[e] = 0x7fffffff;
         is_hit[e] = 0;
@@ -269,11 +273,18 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
         use_slot[d.expert] = d.slot;
         atomicOr(&hit_slot[d.slot >> 5], 1u << (d.slot & 31));
     }
+    {
+        int n = 0;
+        for (int i = tid; i < K; i += nthr) n += g_lu[i] != ~0ull;
+        atomicAdd(&Kl, n);
+    }
     __syncthreads();
+    const int KP = Kl;
     // the untouched slots by ascending last-use stamp (stamps < 2^50, slots < 2^14)
     for (size_t i = tid; i < N; i += nthr)
-        key[i] = (i < (size_t)K && !((hit_slot[i >> 5] >> (i & 31)) & 1u)) ? ((g_lu[i] << 14) | (unsigned long long)i)
-                                                                           : ~0ull;
+        key[i] = (i < (size_t)K && !((hit_slot[i >> 5] >> (i & 31)) & 1u) && g_lu[i] != ~0ull)
+                     ? ((g_lu[i] << 14) | (unsigned long long)i)
+                     : ~0ull;
     __syncthreads();
     for (size_t size = 2; size <= N; size <<= 1)
         for (size_t stride = size >> 1; stride > 0; stride >>= 1) {
@@ -289,24 +300,24 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
             }
             __syncthreads();
         }
-    for (int i = tid; i < K - nh; i += nthr) L0[i] = (int)(key[i] & 0x3fffull);
+    for (int i = tid; i < KP - nh; i += nthr) L0[i] = (int)(key[i] & 0x3fffull);
     // then the hits in touch order (first occurrence), stamped clk + rank
     for (int u = tid; u < nh; u += nthr) {
         const UnitDesc& d = s.units[u];
         int rank = 0;
         for (int v = 0; v < nh; ++v) rank += first[s.units[v].expert] < first[d.expert];
-        L0[K - nh + rank] = d.slot;
+        L0[KP - nh + rank] = d.slot;
     }
     __syncthreads();
     // misses: miss j (ascending, staged unit nh + j) is read from slot L0[j mod K]
     for (int j = tid; j < nm; j += nthr) {
         const int e = s.units[nh + j].expert;
-        const int sl = L0[j % K];
+        const int sl = L0[j % KP];
         use_slot[e] = sl;
         s.copy_slot[j] = sl;
     }
     // evict what the positions that take a miss held before the call
-    const int npos = nm < K ? nm : K;
+    const int npos = nm < KP ? nm : KP;
     for (int i = tid; i < npos; i += nthr) {
         const int old = g_kof[L0[i]];
         if (old >= 0) c.slot_map[old] = -1;
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
     // the last miss placed at each position stays; the hits not displaced keep
     // their touch stamps
     for (int i = tid; i < npos; i += nthr) {
-        const int jl = i + K * ((nm - 1 - i) / K);
+        const int jl = i + KP * ((nm - 1 - i) / KP);
         const int e = s.units[nh + jl].expert;
         const int sl = L0[i];
         g_kof[sl] = layer * E + e;
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
         g_lu[sl] = clk + nh + jl;
     }
     for (int r = tid; r < nh; r += nthr)
-        if (K - nh + r >= npos) g_lu[L0[K - nh + r]] = clk + r;
+        if (KP - nh + r >= npos) g_lu[L0[KP - nh + r]] = clk + r;
     for (int i = tid; i < n_ids; i += nthr) {
         const int e = s.ids[i];
         s.slot_of[i] = use_slot[e];
@@ -332,6 +343,7 @@ __global__ void __launch_bounds__(kPageinThreads) k_pagein(CacheDev c, Scratch s
     __syncthreads();
     if (tid == 0) {
         c.clock[pool] = clk + nh + nm;
+        pl->pool_slots = KP;
         unsigned long long* st = c.stats + a.bucket * 5;
         st[0] += 1;
         st[1] += (unsigned long long)nh;
@@ -349,7 +361,7 @@ __global__ void __launch_bounds__(256) k_pagein_copy(CacheDev c, Scratch s, int 
     griddep_wait();
     const Plan* pl = s.plan;
     const int nm = pl->n_uniq - pl->n_hit;
-    const int keep_from = nm - (nm < c.K ? nm : c.K);
+    const int keep_from = nm - (nm < pl->pool_slots ? nm : pl->pool_slots);
     const int j0 = max(group * G, keep_from), j1 = min(group * G + G, nm);
     if (j0 >= j1) return;
     const int pool = c.pool_mode ? 0 : layer;
@@ -377,6 +389,120 @@ __global__ void __launch_bounds__(256) k_pagein_copy(CacheDev c, Scratch s, int 
         }
     }
 }
+
+// ---------------------------------------------------------------------------
+// Adaptive per-layer capacity: "Running a 95 GiB MoE Model on a 32 GiB GPU"
+// (busyjay.com), "Decode": as decoding progresses, some capacity moves from
+// layers with high hit rates to layers with low hit rates, the total kept.
+// After every decode call; every adapt_period * L calls the layer with the
+// highest hit rate in the window gives adapt_step slots, one at a time, to
+// the layer with the lowest (rates compared exactly as h1 (h2 + m2) against
+// h2 (h1 + m1); lower layer first on ties; no move on equal rates; bounds
+// adapt_kmin .. K places). The moved slot is the giver's least recently used
+// (smallest stamp; its expert evicted, its place left empty with stamp ~0)
+// and becomes the taker's least recently used: its lowest empty place,
+// stamped below every stamp of that pool. One CTA.
+// ---------------------------------------------------------------------------
+constexpr int kAdaptThreads = 256;
+
+__global__ void __launch_bounds__(kAdaptThreads) k_adapt(CacheDev c) {
+    griddep_wait();
+    __shared__ int go, dsel, rsel;
+    __shared__ unsigned long long wv[kAdaptThreads / 32];
+    __shared__ int wi[kAdaptThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = kAdaptThreads / 32;
+    if (tid == 0) {
+        go = 0;
+        const unsigned long long n = *c.adapt_calls + 1;
+        *c.adapt_calls = n;
+        if (n % ((unsigned long long)c.adapt_period * c.L) == 0) {
+            int d = -1, r = -1;
+            for (int l = 0; l < c.L; ++l) {
+                const unsigned long long h = c.win[2 * l], t = h + c.win[2 * l + 1];
+                if (t == 0) continue;
+                if (c.pool_K[l] - c.adapt_step >= c.adapt_kmin) {
+                    const unsigned long long hd = d < 0 ? 0 : c.win[2 * d], td = d < 0 ? 0 : hd + c.win[2 * d + 1];
+                    if (d < 0 || h * td > hd * t) d = l;
+                }
+                if (c.pool_K[l] + c.adapt_step <= c.K) {
+                    const unsigned long long hr = r < 0 ? 0 : c.win[2 * r], tr = r < 0 ? 0 : hr + c.win[2 * r + 1];
+                    if (r < 0 || h * tr < hr * t) r = l;
+                }
+            }
+            if (d >= 0 && r >= 0 && d != r) {
+                const unsigned long long hd = c.win[2 * d], td = hd + c.win[2 * d + 1];
+                const unsigned long long hr = c.win[2 * r], tr = hr + c.win[2 * r + 1];
+                if (hd * tr > hr * td) {
+                    go = 1;
+                    dsel = d;
+                    rsel = r;
+                }
+            }
+            for (int l = 0; l < 2 * c.L; ++l) c.win[l] = 0u;
+        }
+    }
+    __syncthreads();
+    if (!go) return;
+    const int d = dsel, r = rsel, K = c.K;
+    unsigned long long* lud = c.last_use + (size_t)d * K;
+    unsigned long long* lur = c.last_use + (size_t)r * K;
+    for (int mv = 0; mv < c.adapt_step; ++mv) {
+        // the giver's least recently used slot (stamps of slots are distinct)
+        unsigned long long v = ~0ull;
+        int sl = 0x7fffffff;
+        for (int i = tid; i < K; i += kAdaptThreads)
+            if (lud[i] < v) {
+                v = lud[i];
+                sl = i;
+            }
+        // the taker's lowest empty place
+        int fr = 0x7fffffff;
+        for (int i = tid; i < K; i += kAdaptThreads)
+            if (lur[i] == ~0ull) {
+                fr = i;
+                break;
+            }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, off);
+            const int os = __shfl_xor_sync(0xffffffffu, sl, off);
+            if (ov < v || (ov == v && os < sl)) {
+                v = ov;
+                sl = os;
+            }
+            fr = min(fr, __shfl_xor_sync(0xffffffffu, fr, off));
+        }
+        if (lane == 0) {
+            wv[warp] = v;
+            wi[warp] = sl;
+        }
+        __shared__ int wf[kAdaptThreads / 32];
+        if (lane == 0) wf[warp] = fr;
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 1; w < nw; ++w) {
+                if (wv[w] < wv[0] || (wv[w] == wv[0] && wi[w] < wi[0])) {
+                    wv[0] = wv[w];
+                    wi[0] = wi[w];
+                }
+                wf[0] = min(wf[0], wf[w]);
+            }
+            const int s = wi[0], t = wf[0];
+            const int key = c.key_of[(size_t)d * K + s];
+            if (key >= 0) c.slot_map[key] = -1;
+            c.key_of[(size_t)d * K + s] = -1;
+            lud[s] = ~0ull;
+            c.pool_K[d] -= 1;
+            c.key_of[(size_t)r * K + t] = -1;
+            lur[t] = c.floor_stamp[r];
+            c.floor_stamp[r] -= 1;
+            c.pool_K[r] += 1;
+        }
+        __syncthreads();
+    }
+}
+
+void launch_adapt(const CacheDev& c, cudaStream_t st) { k_adapt<<<1, kAdaptThreads, 0, st>>>(c); }
 
 // ---------------------------------------------------------------------------
 // Launch helpers

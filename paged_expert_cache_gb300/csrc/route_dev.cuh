@@ -1202,6 +1202,10 @@ static __device__ void plan_decode(const CacheDev& c, const Scratch& s, const Ro
         pl->n_fill = nmiss;
         pl->n_units = n_units;
         pl->status = 0;
+        if (c.win) {
+            c.win[2 * layer] += (unsigned)nh;
+            c.win[2 * layer + 1] += (unsigned)nmiss;
+        }
         unsigned long long* st = c.stats + a.bucket * 5;
         atomicAdd(st + 0, 1ull);
         atomicAdd(st + 1, (unsigned long long)nh);
@@ -1423,6 +1427,10 @@ static __device__ __forceinline__ void plan_small(const CacheDev& c, const Scrat
                 pl->n_fill = nmiss;
                 pl->n_units = n_units;
                 pl->status = 0;
+                if (c.win) {
+                    c.win[2 * layer] += (unsigned)nh;
+                    c.win[2 * layer + 1] += (unsigned)nmiss;
+                }
                 unsigned long long* st = c.stats + a.bucket * 5;
                 atomicAdd(st + 0, 1ull);
                 atomicAdd(st + 1, (unsigned long long)nh);

@@ -32,7 +32,8 @@ class Setup:
     """A GPU cache plus the workload's device inputs."""
 
     def __init__(self, w, K=None, upload="pull", max_tokens=None, pool_bytes=None, trace=4096, decode="auto",
-                 multi_wave=False, eviction="lru", norm_topk=True, speculate=False, prefill="read_only"):
+                 multi_wave=False, eviction="lru", norm_topk=True, speculate=False, prefill="read_only",
+                 adapt=None):
         import torch
         import paged_expert_cache_gb300 as pec
         self.w = w
@@ -42,7 +43,7 @@ class Setup:
                               pool_bytes=(pool_bytes if pool_bytes is not None else w.pool_bytes),
                               has_shared=w.has_shared, upload_mode=upload, max_tokens=mt,
                               decode=decode, multi_wave=multi_wave, eviction=eviction, norm_topk=norm_topk,
-                              speculate=speculate, prefill=prefill)
+                              speculate=speculate, prefill=prefill, adapt=adapt)
         self.cache = pec.MoECache(cfg)
         buf = None
         for l in range(w.L):
@@ -84,11 +85,12 @@ class Setup:
 class OracleRun:
     """The same calls through the oracle: routing, literal LRU, unpaged layer."""
 
-    def __init__(self, w, slot_bytes, K=None, policy="lru", norm=True, prefill="read_only"):
+    def __init__(self, w, slot_bytes, K=None, policy="lru", norm=True, prefill="read_only", adaptive=None):
         self.w = w
         self.norm = norm
         self.K = pool_slots(w, slot_bytes, K)
-        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy, prefill=prefill)
+        self.cache = oracle.Cache(w.L, w.E, w.pool_mode, self.K, slot_bytes, policy=policy, prefill=prefill,
+                                  adaptive=adaptive)
         self._rec = {}
 
     def record(self, layer, e):

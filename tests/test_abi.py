@@ -26,6 +26,7 @@ def test_config_defaults():
     assert c.eviction == 0  # least recently used
     assert c.speculate == 0  # no speculative next-layer prefetch
     assert c.prefill_mode == 0  # prefill reads the cache without changing it
+    assert c.adapt_period == 0  # fixed per-layer capacity
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -42,6 +43,10 @@ def test_config_defaults():
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, eviction=2), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, speculate=True, upload_mode="memcpy"), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, prefill=2), pec.ERR_INVALID),
+    (dict(L=2, E=16, k=2, H=256, I=128, pool_mode="shared", pool_bytes=196608 * 8, adapt=(1, 1, 0, 0)),
+     pec.ERR_INVALID),
+    (dict(L=2, E=16, k=2, H=256, I=128, slots_per_layer=8, adapt=(1, 1, 9, 12)), pec.ERR_INVALID),
+    (dict(L=2, E=16, k=4, H=256, I=128, slots_per_layer=8, adapt=(1, 1, 3, 12)), pec.ERR_INVALID),
     (dict(L=1, E=16, k=2, H=256, I=128, slots_per_layer=8, prefill="page_in", eviction="lfu"), pec.ERR_INVALID),
 ])
 def test_invalid_configurations_are_refused(kw, status):
