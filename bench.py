@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of each oracle CPU sample")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
+    ap.add_argument("--pool-gb", type=float, default=0.0, help="shared pool size override in GB (profiling runs only)")
     ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
                     help="decode launch mode (auto: one kernel for one- or two-token calls on per-layer pools)")
     ap.add_argument("--eviction", default="lru", choices=["lru", "lfu"],
@@ -358,6 +359,8 @@ def run_ours(args):
         w = scaled(w, L=args.layers)
     if args.slots:
         w = scaled(w, slots_per_layer=args.slots)
+    if args.pool_gb:
+        w = scaled(w, pool_bytes=args.pool_gb * 1e9)
     dev = torch.device("cuda", local)
     cfg = pec.make_config(w.L, w.E, w.k, w.H, w.I, fmt=w.fmt, pool_mode=w.pool_mode,
                           slots_per_layer=w.slots_per_layer, pool_bytes=w.pool_bytes, has_shared=w.has_shared,

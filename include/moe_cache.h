@@ -95,8 +95,9 @@ typedef enum { MOE_UPLOAD_PULL = 0, MOE_UPLOAD_MEMCPY = 1 } moe_upload_mode_t;
  * uploads whose shared-memory layout fits. The three-kernel path runs route,
  * gate/up and down kernels. */
 typedef enum {
-    MOE_DECODE_AUTO = 0,          /* one kernel for calls of one or two tokens on per-layer pools
-                                     (where it measured faster), three kernels otherwise */
+    MOE_DECODE_AUTO = 0,          /* one kernel for calls of one token, and of two tokens on
+                                     per-layer pools (where it measured faster), three kernels
+                                     otherwise */
     MOE_DECODE_THREE_KERNELS = 1, /* always three kernels */
     MOE_DECODE_ONE_KERNEL = 2     /* one kernel for every call that fits */
 } moe_decode_mode_t;

@@ -14,6 +14,7 @@
 
 #include "../../include/moe_cache.h"
 #include "common.cuh"
+#include "decode_policy.h"
 
 struct moe_cache {
     moe_config_t cfg;
@@ -168,6 +169,7 @@ moe_status_t init_tables(moe_cache_t* h) {
     if (h->scr.grid_bar) CK(h, cudaMemset(h->scr.grid_bar, 0, sizeof(unsigned)));
     if (h->scr.err) CK(h, cudaMemset(h->scr.err, 0, sizeof(unsigned)));
     if (h->scr.logit_ctr) CK(h, cudaMemset(h->scr.logit_ctr, 0, 2 * sizeof(unsigned)));
+    if (h->scr.pass_ctr) CK(h, cudaMemset(h->scr.pass_ctr, 0, 2 * sizeof(unsigned)));
     if (d.trace_count) CK(h, cudaMemset(d.trace_count, 0, sizeof(unsigned long long)));
     memset(h->memcpy_upload_ns, 0, sizeof(h->memcpy_upload_ns));
     return MOE_OK;
@@ -392,6 +394,7 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
     DA(s.part, P * d.H);
     DA(s.tok_shift, T);
     DA(s.act_amax, P);
+    DA(s.pass_ctr, 2);
     DA(s.plan, 1);
     DA(s.route_done, 1);
     DA(s.tile_done, (size_t)d.H / 16);
@@ -418,7 +421,8 @@ moe_status_t moe_cache_create(const moe_config_t* cfg, const void* const* expert
         cudaMemset(s.copy_t1, 0, 8) != cudaSuccess || cudaMemset(s.plan, 0, sizeof(moe::Plan)) != cudaSuccess ||
         cudaMemset(s.tiles_done, 0, 4) != cudaSuccess || cudaMemset(s.grid_bar, 0, 4) != cudaSuccess ||
         cudaMemset(s.err, 0, 4) != cudaSuccess || cudaMemset(s.logit_ctr, 0, 8) != cudaSuccess ||
-        cudaMemset(s.tok_shift, 0, T * sizeof(int)) != cudaSuccess || cudaMemset(s.act_amax, 0, P * 4) != cudaSuccess)
+        cudaMemset(s.tok_shift, 0, T * sizeof(int)) != cudaSuccess || cudaMemset(s.act_amax, 0, P * 4) != cudaSuccess ||
+        cudaMemset(s.pass_ctr, 0, 2 * sizeof(unsigned)) != cudaSuccess)
         return bail(MOE_ERR_CUDA, "scratch initialisation failed");
     if (c.upload_mode == MOE_UPLOAD_MEMCPY) {
         e = cudaHostAlloc((void**)&h->host_fill, sizeof(int) * (2 + 2 * U), cudaHostAllocDefault);
@@ -565,18 +569,16 @@ moe_status_t moe_layer_forward(moe_cache_t* h, const void* hidden, int32_t T, co
     // events bracket each launch for profiling)
     const bool pdl = !h->prof_on;
     bool fused = false;
-    // MOE_DECODE_AUTO takes the one-kernel path for calls of one or two tokens on
-    // per-layer pools: measured interleaved on one GPU it is 3-14% faster there
-    // (equal for two Q4_0 tokens), and slower with four tokens or with one pool
-    // shared by every layer, where each CTA's redundant ranking and plan, and
-    // one CTA per SM streaming more units, cost more than the kernel
-    // boundaries saved
-    const int mode = h->cfg.split_decode;
-    const bool one_kernel_pays = mode == MOE_DECODE_ONE_KERNEL || (T <= 2 && d.pool_mode == MOE_POOL_PER_LAYER);
-    // the side stream's kernels run beside the expert kernels, so speculation
-    // takes the three-kernel path (the persistent kernel needs every SM)
-    if (decode && mode != MOE_DECODE_THREE_KERNELS && one_kernel_pays && h->fused_ok && !h->cfg.speculate &&
-        h->cfg.upload_mode == MOE_UPLOAD_PULL && moe::layer_smem_bytes(d, T) > 0) {
+    // the path's rule (and its measured reasons) is in decode_policy.h
+    moe::DecodeCall dc;
+    dc.mode = h->cfg.split_decode;
+    dc.T = T;
+    dc.pool_mode = d.pool_mode;
+    dc.upload_mode = h->cfg.upload_mode;
+    dc.speculate = h->cfg.speculate != 0;
+    dc.fused_ok = h->fused_ok;
+    dc.fits = decode && moe::layer_smem_bytes(d, T) > 0;
+    if (decode && moe::one_kernel_decode(dc)) {
         // the whole call in one persistent kernel
         timed(h, 6, st, [&] { fused = moe::launch_layer(d, h->scr, a, out, bucket, st, pdl); });
         if (!fused) {

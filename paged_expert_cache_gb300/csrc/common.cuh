@@ -103,6 +103,7 @@ struct Scratch {
     int* gemm_count;        // its length
     int* tok_shift;         // [T] power-of-two prescale of each token row (token_shift)
     unsigned* act_amax;     // [P] largest |activation| of each pair, as fp32 bits (act_shift)
+    unsigned* pass_ctr;     // [2] CTAs past the logit wait, and the call's parity (one-kernel decode)
 };
 
 // Device cache state and constants of a handle.
@@ -314,23 +315,40 @@ void launch_gateup(const CacheDev& c, const Scratch& s, const uint16_t* x, int T
 void launch_down(const CacheDev& c, const Scratch& s, float* out, int T, int kind, int group, int G, int units,
                  int bucket, cudaStream_t st, bool pdl);
 
-// cudaLaunchKernelEx with the programmatic-serialization attribute when pdl.
+// cudaLaunchKernelEx with the programmatic-serialization attribute when pdl,
+// and as a cooperative launch (every CTA resident at once, or the launch is
+// refused) when coop.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
-                             Args... args) {
+inline cudaError_t launch_ex_coop(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                                  bool coop, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (coop) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (n) {
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = n;
     }
     return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                             Args... args) {
+    return launch_ex_coop(k, grid, block, smem, st, pdl, false, args...);
 }
 size_t route_smem_bytes(const CacheDev& c, int T);
 // Fused decode layer: the dynamic shared memory a call of T tokens needs, or 0

@@ -325,6 +325,30 @@ __device__ __forceinline__ void down_stage_act(const Scratch& s, int P, int I, u
     }
 }
 
+// The combine of a 16-row output tile for every token: y = sum_j w[t,j] v_j in
+// rank order (an fma chain), v_j = the pick's partial sums over the chunk
+// groups in ascending order, plus the shared expert's. One warp per (token,
+// row): lane j gathers v_j, lane 0 runs the chain in order, so the result is
+// the sequential loop's bit for bit. ps: [chunk groups][P][16]; out: the
+// tile's first row of token 0, tokens H apart.
+__device__ __forceinline__ void combine_rows(const float* ps, const float* wts, int T, int k, int P, int ncg,
+                                             int has_shared, float* __restrict__ out, int H) {
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int i = threadIdx.x >> 5; i < T * 16; i += nw) {
+        const int t = i >> 4, row = i & 15;
+        float v = 0.f;
+        if (lane < k || (lane == k && has_shared)) {
+            const int pair = lane < k ? t * k + lane : T * k + t;
+            for (int cg = 0; cg < ncg; ++cg) v += ps[((size_t)cg * P + pair) * 16 + row];
+        }
+        float y = 0.f;
+        for (int j = 0; j < k; ++j) y = fmaf(wts[t * k + j], __shfl_sync(0xffffffffu, v, j), y);
+        const float vs = __shfl_sync(0xffffffffu, v, k < 32 ? k : 0);
+        if (has_shared) y += vs;
+        if (lane == 0) out[(size_t)t * H + row] = y;
+    }
+}
+
 // Row tile rt of the output for every token: the units' down projections of
 // the staged activations (sd: the call's n_units descriptors in shared
 // memory; ps: [chunk groups][P][16] partials), combined with the router
@@ -407,23 +431,7 @@ __device__ void down_rows_tile(const CacheDev& c, const Scratch& s, const UnitDe
         }
     }
     __syncthreads();
-    for (int i = tid; i < T * 16; i += nthr) {
-        const int t = i >> 4, row = i & 15;
-        float y = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int pair = t * k + j;
-            float v = 0.f;
-            for (int cg = 0; cg < ncg; ++cg) v += ps[((size_t)cg * P + pair) * 16 + row];
-            y = fmaf(wts[pair], v, y);
-        }
-        if (c.has_shared) {
-            const int pair = T * k + t;
-            float v = 0.f;
-            for (int cg = 0; cg < ncg; ++cg) v += ps[((size_t)cg * P + pair) * 16 + row];
-            y += v;
-        }
-        out[(size_t)t * H + (size_t)rt * 16 + row] = y;
-    }
+    combine_rows(ps, wts, T, k, P, ncg, c.has_shared, out + (size_t)rt * 16, H);
     __syncthreads();
 }
 

@@ -43,6 +43,7 @@
 // Waits are bounded: a grid barrier or a slot wait that outlasts its limit
 // sets an error bit the host reports as MOE_ERR_TIMEOUT; the kernel waits
 // (again bounded) for its own copies in flight before it returns.
+#include "decode_policy.h"
 #include "expert_dev.cuh"
 #include "route_dev.cuh"
 
@@ -527,6 +528,13 @@ __device__ __forceinline__ GateUpAcc pull_item(const uint8_t* Wg, uint8_t* Dg, i
     return r;
 }
 
+// A CTA whose wait gave up writes NaN over its share of the output (every
+// G-th block of the CTA size), so a call that could not complete shows in its
+// output, not only in the error bit moe_cache_stats reports.
+__device__ __forceinline__ void poison_out(float* out, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) out[i] = __int_as_float(0x7fc00000);
+}
+
 // kOneToken: the instantiation for one token and at most kLThreads (512)
 // experts, one per thread, with the many-token ranking left out (its
 // registers would crowd the rest).
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     griddep_wait();
     griddep_launch();
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
-    unsigned phase = 0;
+    unsigned phase = 0, call_par = 0;
     {
         // the tokens, and the pool's state if not staged yet
         for (int i = tid; i < T * (H / 8); i += kLThreads) cp_async16(xs + (size_t)i * 8, a.x + (size_t)i * 8);
@@ -616,8 +624,9 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
         // the pairs' activation maxima start from zero; this is ordered before
         // every other CTA's gate/up by the logit announcement (or the grid
         // barrier) below, and after the previous call's readers by the wait
-        if (b == 0)
+        if (b == 0) {
             for (int i = tid; i < P; i += kLThreads) s.act_amax[i] = 0u;
+        }
         for (int i = tid; i < E; i += kLThreads) m.first[i] = 0x7fffffff;
         for (int i = tid; i <= E / 32; i += kLThreads) m.missbits[i] = 0u;
         if (tid == 0) {
@@ -625,6 +634,8 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             unsigned cur;
             asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(cur) : "l"(s.grid_bar) : "memory");
             phase = cur & 0x80000000u;
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(cur) : "l"(s.pass_ctr + 1) : "memory");
+            call_par = cur & 1u;
         }
         cp_async_wait();
         __syncthreads();
@@ -633,7 +644,9 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     // every CTA's ranking, the f16 copy below only this CTA's expert phase
     if (e_mine < E)
         for (int t = 0; t < T; ++t) router_logit_row(c, a, xs + (size_t)t * H, wr, t, e_mine, s.logits, s.bounds);
-    const unsigned parity = phase ? 1u : 0u;  // thread 0: this call's parity (one grid barrier per call)
+    // thread 0: this call's parity, which alternates from call to call (the
+    // last CTA past the logit wait flips it for the next call)
+    const unsigned parity = call_par;
     if (logit_wait && b < NL) {
         __syncthreads();
         if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(s.logit_ctr + parity) : "memory");
@@ -694,9 +707,20 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             lw_ok = good;
         }
         __syncthreads();
-        if (!lw_ok) return;  // nothing is in flight yet
+        if (!lw_ok) {  // nothing is in flight yet
+            poison_out(out, T * H);
+            return;
+        }
+        // the last CTA past the wait clears this parity's counter for the call
+        // two ahead and flips the parity for the next call
+        if (tid == 0 && atomicAdd(s.pass_ctr, 1u) == (unsigned)G - 1) {
+            s.logit_ctr[parity] = 0u;
+            s.pass_ctr[0] = 0u;
+            s.pass_ctr[1] = parity ^ 1u;
+        }
     } else if (!grid_barrier(s.grid_bar, s.err, phase)) {
-        return;  // nothing is in flight yet
+        poison_out(out, T * H);  // nothing is in flight yet
+        return;
     }
 
     // ---- 2. top-k and plan in every CTA ----------------------------------
@@ -881,26 +905,67 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             group_sync(grp);
         }
     }
-    if (!grid_barrier(s.grid_bar, s.err, phase)) {
-        __syncthreads();
-        drain_ring(L, smem, q.n);
-        return;
-    }
-
     // ---- 4. down projection + combine by row tiles -------------------------
-    // every CTA is past its logit wait: clear this parity's counter for the
-    // call two ahead (the next call uses the other one)
-    if (logit_wait && b == 0 && tid == 0) s.logit_ctr[parity] = 0u;
-    if (defer) {
-        // this CTA has no row tile: its ring and staging are free for the plan
+    uint16_t* ah = reinterpret_cast<uint16_t*>(smem + L.ah);
+    uint16_t* al = reinterpret_cast<uint16_t*>(smem + L.al);
+    float* ps = reinterpret_cast<float*>(smem + L.ps);
+    const int ld = I + 8;
+    const int ncg = (KCD + kDRChunks - 1) / kDRChunks;
+    const uint32_t len0 = (uint32_t)KCD * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
+    const int g = lane >> 2, qd = lane & 3;
+    // one (unit, chunk group) item of row tile rt: the unit's partial sums over
+    // its chunk group (pdv: the unit's down rows in the ring)
+    auto down_item = [&](int u, int cgi, const uint8_t* pdv, int rt, uint32_t soff) {
+        const UnitDesc& d = sd[u];
+        const int col = lane & 7;
+        const int pr = col < d.np ? d.pair8[col] : P;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ci = 0; ci < kDRChunks; ++ci) {
+            const int kc = cgi * kDRChunks + ci;
+            if (kc >= KCD) break;
+            Chunk<FMT> ch;
+            if (d.dst) {
+                // a missed record: written to its slot by the gate/up pass
+                load_chunk_cg<FMT>(reinterpret_cast<const uint8_t*>(d.dst) + 2 * mgu, H, I, rt, kc, lane, ch);
+            } else {
+                smem_chunk<FMT>(pdv, len0, soff, kc, lane, ch);
+            }
+            uint32_t bf[2][4][2];
+            const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+            const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
+            ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
+            ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
+            ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
+            ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
+            mma_chunk<FMT, 2>(ch, bf, acc);
+        }
+        const float gd = d.g[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int cc = 2 * qd + c2;
+                if (cc < d.np) {
+                    const int pair = d.pair8[cc];
+                    ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd * pow2f(psh[pair]);
+                }
+            }
+        }
+    };
+    // the committing CTA runs the full plan on a fresh copy of the pool's state
+    // (nothing else writes that state during the call, and every CTA read it
+    // before the logit wait); its ring and staging are free once its own
+    // gate/up is done
+    auto deferred_plan = [&]() {
         stage_state();
         for (int i = tid; i < E; i += kLThreads) m.first[i] = 0x7fffffff;
         for (int i = tid; i <= E / 32; i += kLThreads) m.missbits[i] = 0u;
         cp_async_wait();
         __syncthreads();
         plan_small(c, s, a, m, clk, sids, sd, true);
-    }
-    if (commit && tid == 0) {
+    };
+    auto book_copy_time = [&]() {
         // every miss of the call has been streamed: book the time
         const unsigned long long t1 = atomicAdd(s.copy_t1, 0ull);
         if (t1) {
@@ -909,69 +974,31 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             *s.copy_t0 = ~0ull;
             *s.copy_t1 = 0ull;
         }
+    };
+    if (!grid_barrier(s.grid_bar, s.err, phase)) {
+        __syncthreads();
+        drain_ring(L, smem, q.n);
+        poison_out(out, T * H);
+        return;
     }
+    if (defer) deferred_plan();
+    if (commit && tid == 0) book_copy_time();
     if (q.n_rt > 0) {
-        uint16_t* ah = reinterpret_cast<uint16_t*>(smem + L.ah);
-        uint16_t* al = reinterpret_cast<uint16_t*>(smem + L.al);
-        float* ps = reinterpret_cast<float*>(smem + L.ps);
-        const int ld = I + 8;
-        const int ncg = (KCD + kDRChunks - 1) / kDRChunks;
-        const uint32_t len0 = (uint32_t)KCD * (FMT == FMT_BF16 ? 2048 : (FMT == FMT_FP8_B128 ? 1024 : 512));
         down_stage_act<FMT>(s, P, I, ah, al, psh);
         __syncthreads();
-        const int g = lane >> 2, qd = lane & 3;
         for (int r = 0; r < q.n_rt; ++r) {
             const int rt = b + G * r;
             const uint32_t soff = scale_soff<FMT>(H, I, rt);
-            // one (unit, chunk group) item: the unit's partial sums of this row
-            // tile over its chunk group (pdv: the unit's down rows in the ring)
-            auto down_item = [&](int u, int cgi, const uint8_t* pdv) {
-                const UnitDesc& d = sd[u];
-                const int col = lane & 7;
-                const int pr = col < d.np ? d.pair8[col] : P;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ci = 0; ci < kDRChunks; ++ci) {
-                    const int kc = cgi * kDRChunks + ci;
-                    if (kc >= KCD) break;
-                    Chunk<FMT> ch;
-                    if (d.dst) {
-                        // a missed record: written to its slot by the gate/up pass
-                        load_chunk_cg<FMT>(reinterpret_cast<const uint8_t*>(d.dst) + 2 * mgu, H, I, rt, kc, lane, ch);
-                    } else {
-                        smem_chunk<FMT>(pdv, len0, soff, kc, lane, ch);
-                    }
-                    uint32_t bf[2][4][2];
-                    const uint16_t* rh = ah + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
-                    const uint16_t* rl = al + (size_t)pr * ld + kc * 64 + (lane >> 3) * 8;
-                    ldmatrix_x4(bf[0][0][0], bf[0][0][1], bf[0][1][0], bf[0][1][1], rh);
-                    ldmatrix_x4(bf[0][2][0], bf[0][2][1], bf[0][3][0], bf[0][3][1], rh + 32);
-                    ldmatrix_x4(bf[1][0][0], bf[1][0][1], bf[1][1][0], bf[1][1][1], rl);
-                    ldmatrix_x4(bf[1][2][0], bf[1][2][1], bf[1][3][0], bf[1][3][1], rl + 32);
-                    mma_chunk<FMT, 2>(ch, bf, acc);
-                }
-                const float gd = d.g[2];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const int cc = 2 * qd + c2;
-                        if (cc < d.np) {
-                            const int pair = d.pair8[cc];
-                            ps[((size_t)cgi * P + pair) * 16 + g + 8 * h2] = acc[2 * h2 + c2] * gd * pow2f(psh[pair]);
-                        }
-                    }
-                }
-            };
-            if (q.n <= L.ns) {
-                // every piece was requested at the start and no slot is
-                // refilled: all units' items in one pass, each waiting for
-                // its own piece
+            if (q.n_rt * q.dpr <= L.ns) {
+                // the down pieces take distinct slots, and each was issued by
+                // the end of gate/up (at the start, or as the refill of a
+                // gate/up piece), so no slot is refilled here: all units'
+                // items in one pass, each waiting for its own piece
                 for (int itm = warp; itm < n_units * ncg; itm += kLWarps) {
                     const int u = itm / ncg, cgi = itm - u * ncg, pc = u / L.m;
                     const int i = q.n_gu + r * q.dpr + pc;
                     if (!ring_wait(L, smem, i)) slot_err = 1;
-                    down_item(u, cgi, ring + (size_t)(i % L.ns) * L.slot + (size_t)(u - pc * L.m) * L.du);
+                    down_item(u, cgi, ring + (size_t)(i % L.ns) * L.slot + (size_t)(u - pc * L.m) * L.du, rt, soff);
                 }
                 __syncthreads();
             } else {
@@ -984,30 +1011,14 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
                     const uint8_t* pd = ring + (size_t)slot * L.slot;
                     for (int itm = warp; itm < nup * ncg; itm += kLWarps) {
                         const int v = itm / ncg, cgi = itm - v * ncg;
-                        down_item(u0 + v, cgi, pd + (size_t)v * L.du);
+                        down_item(u0 + v, cgi, pd + (size_t)v * L.du, rt, soff);
                     }
                     __syncthreads();
                     // the slot is consumed: refill it with the piece ns ahead
                     if (tid == 0 && i + L.ns < q.n) issue_piece<FMT>(i + L.ns, q, L, sd, smem, H, I, pol);
                 }
             }
-            for (int i = tid; i < T * 16; i += kLThreads) {
-                const int t = i >> 4, row = i & 15;
-                float y = 0.f;
-                for (int j = 0; j < k; ++j) {
-                    const int pair = t * k + j;
-                    float v = 0.f;
-                    for (int cgi = 0; cgi < ncg; ++cgi) v += ps[((size_t)cgi * P + pair) * 16 + row];
-                    y = fmaf(swts[pair], v, y);
-                }
-                if (c.has_shared) {
-                    const int pair = T * k + t;
-                    float v = 0.f;
-                    for (int cgi = 0; cgi < ncg; ++cgi) v += ps[((size_t)cgi * P + pair) * 16 + row];
-                    y += v;
-                }
-                out[(size_t)t * H + (size_t)rt * 16 + row] = y;
-            }
+            combine_rows(ps, swts, T, k, P, ncg, c.has_shared, out + (size_t)rt * 16, H);
             __syncthreads();
         }
     }
@@ -1059,8 +1070,18 @@ static bool layer_launch_as(const CacheDev& c, const Scratch& s, const RouteArgs
             cudaSuccess ||
         per_sm < 1)
         return false;
-    return launch_ex(k_layer<FMT, kOneToken>, dim3(layer_ctas()), dim3(kLThreads), sm, st, pdl, c, s, a, out) ==
-           cudaSuccess;
+    // a cooperative launch (the runtime starts the grid only when every CTA can
+    // be resident, which the grid-wide waits need), with programmatic
+    // dependent launch first
+    static int form = kCoopWithPdl;
+    const dim3 grid(layer_ctas()), block(kLThreads);
+    return launch_cooperative(form, pdl, [&](bool with_pdl) {
+        if (launch_ex_coop(k_layer<FMT, kOneToken>, grid, block, sm, st, with_pdl, true, c, s, a, out) ==
+            cudaSuccess)
+            return true;
+        cudaGetLastError();
+        return false;
+    });
 }
 
 template <int FMT>
