@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; not a bench number)")
     ap.add_argument("--slots", type=int, default=0, help="slots per layer override (profiling runs only)")
     ap.add_argument("--pool-gb", type=float, default=0.0, help="shared pool size override in GB (profiling runs only)")
+    ap.add_argument("--prime", type=int, default=PRIME,
+                    help="untimed decode steps that fill the cache before the warm-up (more: profiling runs only)")
     ap.add_argument("--decode", default="auto", choices=["auto", "three_kernels", "one_kernel"],
                     help="decode launch mode (auto: one kernel for one- or two-token calls on per-layer pools)")
     ap.add_argument("--eviction", default="lru", choices=["lru", "lfu"],
@@ -381,9 +383,9 @@ def run_ours(args):
     if args.speculate:
         for l in range(w.L):
             cache.set_router(l, routers[l], bias)
-    # the cache is primed with PRIME decode steps of the same streams before
+    # the cache is primed with args.prime decode steps of the same streams before
     # the warm-up, so the timed steps see the steady-state hit rate whatever W is
-    n_total = PRIME + args.warmup + args.steps + args.profile_steps
+    n_total = args.prime + args.warmup + args.steps + args.profile_steps
     hid = np.empty((n_total, w.L, T, w.H), dtype=np.uint16)
     for l in range(w.L):
         for s in range(T):
@@ -422,7 +424,7 @@ def run_ours(args):
 
     # priming (eager; also sets every kernel attribute before capture), then
     # the capture of one step, then the warm-up steps through the graph
-    for _ in range(PRIME):
+    for _ in range(args.prime):
         next_inputs()
         step_layers()
     torch.cuda.synchronize()
@@ -448,7 +450,7 @@ def run_ours(args):
         nonlocal cursor
         cache.reset()
         cursor = 0
-        for _ in range(PRIME):
+        for _ in range(args.prime):
             next_inputs()
             step_layers()
         for _ in range(args.warmup):
@@ -495,7 +497,7 @@ def run_ours(args):
     # timed window (the cache is deterministic), so the window replays exactly
     # the timed window's cache transactions, hits and misses, with the host
     # copies added.
-    e0_step = PRIME + args.warmup
+    e0_step = args.prime + args.warmup
     h_in = torch.from_numpy(hid[e0_step:e0_step + args.steps].view(np.int16)).pin_memory()
     h_out = torch.empty((w.L, T, w.H), dtype=torch.float32).pin_memory()
     reprime()
@@ -521,7 +523,7 @@ def run_ours(args):
     e2e_ms, _ = aggregate(e0.elapsed_time(e1), args.steps * T, dist, dev)
     e_s1 = cache.stats()["buckets"][bk]
     e2e_same_misses = (e_s1["misses"] - e_s0["misses"]) == misses and (e_s1["hits"] - e_s0["hits"]) == hits
-    cursor = PRIME + args.warmup + args.steps
+    cursor = args.prime + args.warmup + args.steps
 
     # Per-launch device time of every stage, call by call over further steps of
     # the same streams: a spin kernel ahead of each call lets the host enqueue
@@ -673,7 +675,7 @@ def run_ours(args):
                             "are inside the timed region"} if args.chained else None,
         "run": {"pool_gb": info["pool_device_bytes"] / 1e9, "store_gb": info["store_host_bytes"] / 1e9,
                 "parallelism": f"replicas x{world}", "cuda_graph": graph is not None,
-                "cache_priming_steps": PRIME, "decode_mode": args.decode, "speculate": args.speculate,
+                "cache_priming_steps": args.prime, "decode_mode": args.decode, "speculate": args.speculate,
                 "adapt_period": args.adapt, "pool_slots_at_end": cache.pool_slots() if args.adapt else None,
                 "clock_sample_ms": args.clock_ms},
         "hit_rate": hits / max(1, hits + misses), "misses_per_token": misses / max(1, args.steps * T),
@@ -727,6 +729,8 @@ def run_prefill(args):
         w = WORKLOADS["flash_next_prefill"]  # the workload that has a prompt
     if args.layers:
         w = scaled(w, L=args.layers)
+    if args.pool_gb:
+        w = scaled(w, pool_bytes=args.pool_gb * 1e9)
     T = w.prompt_T
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
@@ -748,12 +752,12 @@ def run_prefill(args):
                            for l in range(w.L)]).to(dev)
     out = torch.empty((T, w.H), dtype=torch.float32, device=dev)
     # decode steps of batch 1 leave a working set resident, as after a chat turn
-    xs = [torch.from_numpy(synth.hidden_ar1(w.seed, l, 0, PRIME, w.H, w.rho).view(np.int16)).to(dev)
+    xs = [torch.from_numpy(synth.hidden_ar1(w.seed, l, 0, args.prime, w.H, w.rho).view(np.int16)).to(dev)
           for l in range(w.L)]
     dec_out = torch.empty((1, w.H), dtype=torch.float32, device=dev)
 
     def prime_decode():
-        for s_ in range(PRIME):
+        for s_ in range(args.prime):
             for l in range(w.L):
                 cache.forward(xs[l][s_:s_ + 1], routers[l], l, dec_out, bias=bias, T=1)
         torch.cuda.synchronize()
@@ -825,7 +829,7 @@ def run_prefill(args):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 tcgen05 products, fp32 accumulate in tensor memory", "data": "synthetic",
         "config": {"workload": w.name, "prompt_tokens": T, "layers": w.L, "experts": w.E, "top_k": w.k,
-                   "format": w.fmt, "prefill_group": 32, "priming_decode_steps": PRIME,
+                   "format": w.fmt, "prefill_group": 32, "priming_decode_steps": args.prime,
                    "prefill_mode": "page_in" if args.page_in else "read_only"},
         "first_prompt_pass": {"ms": ttft_med[0], "experts_staged": ttft_med[1], "experts_resident": ttft_med[2],
                               "bytes_over_link": ttft_med[1] * cache.info()["slot_bytes"],

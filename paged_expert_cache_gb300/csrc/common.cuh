@@ -204,10 +204,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
     return (uint32_t)r.x | ((uint32_t)r.y << 16);
 }
 
-// Two e2m1 codes in one byte (low nibble = lower column) -> fp16x2, exact.
-__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
-    __half2_raw r = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(byte & 0xffu), __NV_E2M1);
-    return (uint32_t)r.x | ((uint32_t)r.y << 16);
+// The fp16x2 bits of two e2m1 codes (sign, 2 exponent bits, 1 mantissa bit)
+// held at bits 0-3 (low half) and 16-19 (high half) of x, scaled by 2^-14:
+// the code's 3 magnitude bits placed at fp16 bits 9-11 are its value's
+// exponent and mantissa with fp16's bias 15 instead of e2m1's 1 (normal codes),
+// or its subnormal (code 1 -> 2^-15 = 0.5 * 2^-14), and its sign goes to bit
+// 15. Exact, and plain integer work: the hardware's e2m1 conversion runs on a
+// pipe with a fraction of the integer rate.
+__device__ __forceinline__ uint32_t e2m1x2_bits_2m14(uint32_t x) {
+    return ((x << 9) & 0x0E000E00u) | ((x << 12) & 0x80008000u);
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
@@ -216,6 +221,33 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// Asynchronous global -> shared copies of 4, 8 or 16 bytes (completed by
+// cp_async_wait).
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;\n" ::: "memory");
+}
+// Closes the current group of asynchronous copies.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// Waits for every group but the most recently committed one.
+__device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+// Asks L2 for `bytes` from `src` (16-byte aligned, a multiple of 16) without
+// copying them anywhere, so later reads of them hit L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint2 ldg_stream8(const void* p) {

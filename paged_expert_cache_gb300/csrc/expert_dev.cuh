@@ -60,6 +60,42 @@ __device__ __forceinline__ void load_chunk(const uint8_t* M, uint8_t* D, int R, 
     }
 }
 
+// Asks L2 for row tiles rt0 .. rt0 + nrt - 1 of a slot matrix (R rows, C
+// columns) whole: their codes are one contiguous range and so are their
+// scales (block-FP8: the 128-row blocks of scales they use). Thread `part` of
+// nparts issues its share of 16 KB pieces.
+template <int FMT>
+__device__ __forceinline__ void prefetch_rows(const uint8_t* M, int R, int C, int rt0, int nrt, int part, int nparts) {
+    const int KC = C / 64;
+    uint64_t off[2], len[2];
+    int nr = 1;
+    if constexpr (FMT == FMT_Q4_0 || FMT == FMT_NVFP4) {
+        off[0] = (uint64_t)rt0 * KC * 512;
+        len[0] = (uint64_t)nrt * KC * 512;
+        off[1] = (uint64_t)R * C / 2 + (uint64_t)rt0 * KC * 64;
+        len[1] = (uint64_t)nrt * KC * 64;
+        nr = 2;
+    } else if constexpr (FMT == FMT_FP8_B128) {
+        const int nct = (C + 127) / 128;
+        off[0] = (uint64_t)rt0 * KC * 1024;
+        len[0] = (uint64_t)nrt * KC * 1024;
+        const uint64_t s0 = (uint64_t)R * C + (uint64_t)((rt0 * 16) / 128) * nct * 4;
+        const uint64_t s1 = (uint64_t)R * C + (uint64_t)((rt0 * 16 + nrt * 16 + 127) / 128) * nct * 4;
+        off[1] = s0 & ~15ull;
+        len[1] = ((s1 + 15) & ~15ull) - off[1];
+        nr = 2;
+    } else {
+        off[0] = (uint64_t)rt0 * KC * 2048;
+        len[0] = (uint64_t)nrt * KC * 2048;
+    }
+    constexpr uint64_t kPiece = 16384;
+    int idx = 0;
+    for (int r = 0; r < nr; ++r)
+        for (uint64_t o = 0; o < len[r]; o += kPiece, ++idx)
+            if (idx % nparts == part)
+                prefetch_l2(M + off[r] + o, (uint32_t)(len[r] - o < kPiece ? len[r] - o : kPiece));
+}
+
 // The same loads through L2 only, for a record written earlier in the running
 // grid (the read-only path may not see such writes).
 template <int FMT>
@@ -119,20 +155,28 @@ __device__ __forceinline__ void mma_chunk(const Chunk<FMT>& ch, const uint32_t (
             acc[3] = fmaf(dr8, t[3], acc[3]);
         }
     } else if constexpr (FMT == FMT_NVFP4) {
+        // A = code * 2^-14 (its bits, e2m1x2_bits_2m14) times scale * 2^7:
+        // code * scale * 2^-7, exact in fp16 (at most 6 significant bits, and at
+        // least 2^-17 when not zero); the chunk's sum is scaled back by 2^7,
+        // exactly, as it is added
         const uint32_t w[4] = {ch.q.x, ch.q.y, ch.q.z, ch.q.w};
+        const __half2 k7 = __float2half2_rn(128.0f);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             const uint32_t scw = s < 2 ? ch.sc.x : ch.sc.y;
-            const __half2 sh = u32_as_h2(e4m3x2_to_h2((scw >> (16 * (s & 1))) & 0xffffu));
+            const __half2 sh = __hmul2(u32_as_h2(e4m3x2_to_h2((scw >> (16 * (s & 1))) & 0xffffu)), k7);
             const __half2 sg = __low2half2(sh), s8 = __high2half2(sh);
             uint32_t a[4];
-            a[0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(w[s] & 0xffu)), sg));
-            a[1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[s] >> 8) & 0xffu)), s8));
-            a[2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[s] >> 16) & 0xffu)), sg));
-            a[3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(w[s] >> 24)), s8));
+            a[0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s])), sg));
+            a[1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 4)), s8));
+            a[2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 8)), sg));
+            a[3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 12)), s8));
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_f16(acc, a, b[nb][s][0], b[nb][s][1]);
+            for (int nb = 0; nb < NB; ++nb) mma_f16(t, a, b[nb][s][0], b[nb][s][1]);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(128.0f, t[i], acc[i]);
     } else if constexpr (FMT == FMT_FP8_B128) {
         const uint32_t w[8] = {ch.q0.x, ch.q0.y, ch.q0.z, ch.q0.w, ch.q1.x, ch.q1.y, ch.q1.z, ch.q1.w};
         float t[4] = {0.f, 0.f, 0.f, 0.f};

@@ -134,10 +134,15 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2);
 }
 
+// The GEMM's fp16 weights are the true ones divided by gemm_wscale (NVFP4: by
+// 2^7, so one multiply builds them exactly); the epilogues multiply by it.
+template <int FMT>
+__host__ __device__ constexpr float gemm_wscale() { return FMT == FMT_NVFP4 ? 128.0f : 1.0f; }
+
 // ---------------------------------------------------------------------------
 // Weight fragments -> fp16 (fragment order of load_chunk: lane (g, q), k-step
 // s holds (row g, cols 16s+2q..+1), (row g+8, same), (row g, cols 16s+2q+8..+9),
-// (row g+8, same)).
+// (row g+8, same)), divided by gemm_wscale.
 // ---------------------------------------------------------------------------
 template <int FMT>
 __device__ __forceinline__ void frag_to_f16(const Chunk<FMT>& ch, uint32_t (&a)[4][4]) {
@@ -159,13 +164,16 @@ __device__ __forceinline__ void frag_to_f16(const Chunk<FMT>& ch, uint32_t (&a)[
         const uint32_t w[4] = {ch.q.x, ch.q.y, ch.q.z, ch.q.w};
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
+            // code * 2^-14 (its bits) times scale * 2^7: the weight times 2^-7,
+            // exact in fp16; the epilogues scale the sums back (gemm_wscale)
             const uint32_t scw = s < 2 ? ch.sc.x : ch.sc.y;
-            const __half2 sh = u32_as_h2(e4m3x2_to_h2((scw >> (16 * (s & 1))) & 0xffffu));
+            const __half2 sh = __hmul2(u32_as_h2(e4m3x2_to_h2((scw >> (16 * (s & 1))) & 0xffffu)),
+                                       __float2half2_rn(128.0f));
             const __half2 sg = __low2half2(sh), s8 = __high2half2(sh);
-            a[s][0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(w[s] & 0xffu)), sg));
-            a[s][1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[s] >> 8) & 0xffu)), s8));
-            a[s][2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[s] >> 16) & 0xffu)), sg));
-            a[s][3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(w[s] >> 24)), s8));
+            a[s][0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s])), sg));
+            a[s][1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 4)), s8));
+            a[s][2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 8)), sg));
+            a[s][3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_bits_2m14(w[s] >> 12)), s8));
         }
     } else if constexpr (FMT == FMT_FP8_B128) {
         const uint32_t w[8] = {ch.q0.x, ch.q0.y, ch.q0.z, ch.q0.w, ch.q1.x, ch.q1.y, ch.q1.z, ch.q1.w};
@@ -297,6 +305,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
     // token rows j = i / 8 + 32 r, 16-byte column chunk i % 8, r = 0..3
     constexpr int kTokPerThread = kGN * 8 / kGThreads;
     const int rt = m * (kGM / 16) + warp;
+    // the item's whole weight tiles into L2 first: the register pipeline below
+    // holds one chunk in flight, and its loads then wait on L2, not HBM
+    if (warp == 0) {
+        prefetch_rows<FMT>(Wg, I, H, m * (kGM / 16), kGM / 16, lane, 32);
+        prefetch_rows<FMT>(Wu, I, H, m * (kGM / 16), kGM / 16, lane, 32);
+    }
     Chunk<FMT> cg, cu;
     uint4 xv[kTokPerThread];
     auto load_next = [&](int kc) {
@@ -376,7 +390,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_gateup(CacheDev c, Scratc
                 const int p = pairs[col + j];
                 mx[j] = 0u;
                 if (p >= 0) {
-                    const float av = swiglu_scaled(__uint_as_float(g[j]), __uint_as_float(u[j]), d.g[0], d.g[1],
+                    const float av = swiglu_scaled(__uint_as_float(g[j]), __uint_as_float(u[j]),
+                                                   d.g[0] * gemm_wscale<FMT>(), d.g[1] * gemm_wscale<FMT>(),
                                                    pow2f(tsh[col + j]));
                     s.act[(size_t)p * I + i_out] = av;
                     mx[j] = __float_as_uint(fabsf(av));
@@ -451,6 +466,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
     // and activations are in flight while chunk kc is staged
     constexpr int kActPerThread = kGN * 8 / kGThreads;
     const int rt = m * (kGM / 16) + warp;
+    if (warp == 0) prefetch_rows<FMT>(Wd, H, I, m * (kGM / 16), kGM / 16, lane, 32);  // as in gate/up
     Chunk<FMT> ch;
     float4 av[kActPerThread][2];
     auto load_next = [&](int kc) {
@@ -535,7 +551,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_down(CacheDev c, Scratch 
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int p = pairs[col + j];
-                if (p >= 0) s.part[(size_t)p * H + h_out] = __uint_as_float(v[j]) * d.g[2] * pow2f(psh[col + j]);
+                if (p >= 0)
+                    s.part[(size_t)p * H + h_out] =
+                        __uint_as_float(v[j]) * (d.g[2] * gemm_wscale<FMT>()) * pow2f(psh[col + j]);
             }
         }
     }

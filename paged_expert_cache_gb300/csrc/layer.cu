@@ -179,23 +179,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned* ctr, unsigned* err, unsig
     return ok != 0;
 }
 
-// Asynchronous global -> shared copies of 4, 8 or 16 bytes (completed by
-// cp_async_wait).
-__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_all;\n" ::: "memory");
-}
 
 // ---------------------------------------------------------------------------
 // Slot ring: mbarriers and bulk copies (sm_90+ PTX).
@@ -609,7 +592,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             for (int i = tid; i < E * 3; i += kLThreads) cp_async4(m.gl + i, c.gtable + (size_t)a.layer * E * 3 + i);
             if (tid < 3) cp_async4(m.gl + E * 3 + tid, c.gtable + ((size_t)c.L * E + a.layer) * 3 + tid);
         }
-        if (tid == 0) clk = c.clock[pool];
+        if (tid == 0) cp_async8(&clk, c.clock + pool);
     };
     if (a.early) stage_state();
     griddep_wait();
@@ -618,8 +601,13 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     unsigned phase = 0, call_par = 0;
     {
         // the tokens, and the pool's state if not staged yet
+        // two groups: the tokens (with the router rows and any early state),
+        // which the logits wait for, and the state, which only the ranking
+        // and the plan need
         for (int i = tid; i < T * (H / 8); i += kLThreads) cp_async16(xs + (size_t)i * 8, a.x + (size_t)i * 8);
+        cp_async_commit();
         if (!a.early) stage_state();
+        cp_async_commit();
         if (tid < kLayerMaxTokens) tmax[tid] = 0u;
         // the pairs' activation maxima start from zero; this is ordered before
         // every other CTA's gate/up by the logit announcement (or the grid
@@ -637,7 +625,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(cur) : "l"(s.pass_ctr + 1) : "memory");
             call_par = cur & 1u;
         }
-        cp_async_wait();
+        cp_async_wait_but_last();
         __syncthreads();
     }
     // the logits first, announced as soon as they are written: they gate
@@ -686,6 +674,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
         }
         for (int i = tid; i < ldx / 2; i += kLThreads) reinterpret_cast<uint32_t*>(xg + (size_t)T * ldx)[i] = 0u;
     }
+    cp_async_wait();  // the pool's state (made visible by the barriers below)
     if (logit_wait) {
         // every CTA waits until all NL logit CTAs have announced theirs
         __shared__ int lw_ok;

@@ -67,7 +67,11 @@ void repack_nvfp4(const uint8_t* src, int R, int C, uint8_t* dst) {
     const uint8_t* sscales = src + (size_t)R * C / 2;  // [R][C/16]
     uint8_t* codes = dst;
     uint8_t* scales = dst + (size_t)R * C / 2;
-    auto pairbyte = [&](int r, int c) { return scodes[(size_t)r * (C / 2) + c / 2]; };
+    // e2m1 code of (r, c): low nibble of its byte for even c, high for odd
+    auto nib = [&](int r, int c) -> uint32_t {
+        const uint8_t v = scodes[(size_t)r * (C / 2) + c / 2];
+        return (c & 1) ? (uint32_t)(v >> 4) : (uint32_t)(v & 15);
+    };
     auto sc = [&](int r, int b) { return sscales[(size_t)r * (C / 16) + b]; };
     for (int rt = 0; rt < RT; ++rt)
         for (int kc = 0; kc < KC; ++kc) {
@@ -76,12 +80,14 @@ void repack_nvfp4(const uint8_t* src, int R, int C, uint8_t* dst) {
                 const int g = lane >> 2, qd = lane & 3;
                 const int r0 = rt * 16 + g, r8 = r0 + 8;
                 for (int s = 0; s < 4; ++s) {
+                    // the Q4_0 word layout: fragment half2 j from the codes at
+                    // bits 4j (low half) and 4j + 16 (high half), so one shift
+                    // and two masks build its fp16 bits
                     const int c0 = kc * 64 + s * 16 + 2 * qd;
-                    uint8_t* p = codes + (tile * 32 + lane) * 16 + s * 4;
-                    p[0] = pairbyte(r0, c0);
-                    p[1] = pairbyte(r8, c0);
-                    p[2] = pairbyte(r0, c0 + 8);
-                    p[3] = pairbyte(r8, c0 + 8);
+                    const uint32_t w = nib(r0, c0) | (nib(r0, c0 + 1) << 16) | (nib(r8, c0) << 4) |
+                                       (nib(r8, c0 + 1) << 20) | (nib(r0, c0 + 8) << 8) | (nib(r0, c0 + 9) << 24) |
+                                       (nib(r8, c0 + 8) << 12) | (nib(r8, c0 + 9) << 28);
+                    wr32(codes + (tile * 32 + lane) * 16 + s * 4, w);
                 }
             }
             for (int g = 0; g < 8; ++g) {
