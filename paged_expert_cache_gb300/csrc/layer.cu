@@ -800,10 +800,15 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     const uint64_t mgu = matrix_stride(FMT, I, H);
     const Pieces q = make_pieces(b, G, RT, RTD, n_units, L.m);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0 && warp < q.n && warp < L.ns) {
-        // lane 0 of warp w issues piece w, so the first pieces of both groups
-        // are requested at once; the ring reuses shared memory the generic
-        // proxy wrote in phases 1-2
+    // The ring's first fill: piece p < n0 goes into slot p. The first piece of
+    // each group is requested now; piece p >= 2 when its group's item p - 2
+    // has landed, so the first pieces do not queue behind the whole fill and
+    // the groups start computing while the rest streams in (a piece no gate/up
+    // item of its group precedes is requested now too).
+    const int n0 = min(q.n, L.ns);
+    if (lane == 0 && warp < n0 && (warp < 2 || warp - 2 >= q.n_gu)) {
+        // lane 0 of warp w issues piece w; the ring reuses shared memory the
+        // generic proxy wrote in phases 1-2
         fence_proxy_async();
         issue_piece<FMT>(warp, q, L, sd, smem, H, I, pol);
     }
@@ -832,6 +837,10 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
             // a slot may only be refilled once its current piece has been
             // issued, that is once the piece before it was consumed
             if (!ring_wait(L, smem, j)) slot_err = 1;
+            if (gtid == 0 && j + 2 < n0) {  // the group's piece two ahead, of the first fill
+                fence_proxy_async();
+                issue_piece<FMT>(j + 2, q, L, sd, smem, H, I, pol);
+            }
             if (!Dg) {
                 // resident: the tile is in slot j % ns
                 const uint8_t* pg = ring + (size_t)slot * L.slot;
