@@ -715,13 +715,13 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     // ---- 2. top-k and plan in every CTA ----------------------------------
     if (kOneToken) {
         // one token: every expert's key held by its own thread, ranked by
-        // rounds in every warp at once and one merge
+        // counting (up to 256 experts) or by a threshold selection
         const TopkSmem tw = topk_layout(smem + L.topk, E);
         if (E <= 256)
             topk_rank_block(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
                             reinterpret_cast<float2*>(smem + L.rk + (size_t)E * 8), &rerank, sids, swts);
         else
-            topk_block_rounds(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
+            topk_block_select(c, s, a, tw, reinterpret_cast<unsigned long long*>(smem + L.rk),
                               reinterpret_cast<float2*>(smem + L.rk + (size_t)(kLThreads / 32) * kMaxTopK * 8),
                               &rerank, sids, swts);
     } else {

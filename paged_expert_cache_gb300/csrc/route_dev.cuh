@@ -613,23 +613,37 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long ke
     return ((unsigned long long)mhi << 32) | __reduce_max_sync(0xffffffffu, lo);
 }
 
-// Top-k of token 0 by the whole CTA (E <= blockDim.x, k <= kMaxTopK): thread e
-// builds expert e's key (the orderable 64-bit key of topk_token_fast: the
-// logit's high part, then its low part with 1023 - e in the low bits, so keys
-// are distinct). Each warp takes the k largest keys of its 32 experts by k
-// rounds of a warp-wide maximum, in order, into wl [warps][kMaxTopK]; warp 0
-// then merges the warps' sorted lists by k rounds of a maximum over the
-// lists' heads. The picks are the k largest keys in descending order, those
-// of the sorted-list rounds. The certificate is topk_token_fast's (each pick's
-// lower bound above the upper bound of everything ranked after it), checked by
-// every expert against the picks ranked above it and combined with one
-// block-wide AND; warp 0 then weighs as topk_token_fast does, or re-ranks
-// exactly. Every thread of the CTA calls it; lowb: k entries of shared memory.
-static __device__ void topk_block_rounds(const CacheDev& c, const Scratch& s, const RouteArgs& a, const TopkSmem& w,
+// Candidates the threshold selection of topk_block_select ranks itself; with
+// more it falls back to the sorted-list merge.
+constexpr int kBlockCandMax = 128;
+
+// Top-k of token 0 by the whole CTA (E <= blockDim.x <= 32 kMaxTopK, k <=
+// kMaxTopK): thread e builds expert e's key (the orderable 64-bit key of
+// topk_token_fast: the logit's high part, then its low part with 1023 - e in
+// the low bits, so keys are distinct and nonzero).
+//   Threshold selection: L, the k-th largest of the warps' largest keys, is
+//   at most the k-th largest key overall (k warp maxima are >= L), so every
+//   pick has a key >= L. The keys >= L are gathered as candidates (about 16 of
+//   512 for random logits); each candidate's rank is the number of candidates
+//   above it, which for a pick is its rank among all keys. Ranks below k are
+//   the picks, in descending order.
+//   With more than kBlockCandMax candidates, the sorted-list merge: each warp
+//   takes its k largest keys by k rounds of a warp-wide maximum into wl
+//   [warps][kMaxTopK], and warp 0 merges the lists by k rounds over their heads.
+// Both give the k largest keys in order. The certificate is topk_token_fast's
+// (each pick's lower bound above the upper bound of everything ranked after
+// it), checked by every expert against the picks ranked above it and combined
+// with one block-wide AND; warp 0 then weighs as topk_token_fast does, or
+// re-ranks exactly. Every thread of the CTA calls it; lowb: k entries of shared
+// memory; the candidates use w.z64 (E >= kBlockCandMax entries, free until
+// the exact re-rank).
+static __device__ void topk_block_select(const CacheDev& c, const Scratch& s, const RouteArgs& a, const TopkSmem& w,
                                          unsigned long long* wl, float2* lowb, int* rerank_flag, int* ids_out,
                                          float* wts_out) {
     const int E = c.E, k = c.k, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nw = (int)(blockDim.x >> 5);
+    __shared__ unsigned long long wmax[kMaxTopK * 2];
+    __shared__ int ncand;
     unsigned long long key = 0ull;
     if (tid < E) {
         const float2 z = __ldcg(s.logits + tid);
@@ -638,36 +652,84 @@ static __device__ void topk_block_rounds(const CacheDev& c, const Scratch& s, co
         key = ((unsigned long long)ord32(z.x) << 32) |
               (unsigned long long)((ord32(__fadd_rn(z.y, 0.0f)) & ~1023u) | (unsigned)(1023 - tid));
     }
-    // 1. each warp's k largest keys, in order (a popped key becomes zero)
     {
-        unsigned long long mine = key;
-#pragma unroll 1
-        for (int j = 0; j < k; ++j) {
-            const unsigned long long best = warp_max_key(mine);
-            if (lane == 0) wl[warp * kMaxTopK + j] = best;
-            if (mine == best) mine = 0ull;
-        }
+        const unsigned long long m = warp_max_key(key);
+        if (lane == 0) wmax[warp] = m;
+        if (tid == 0) ncand = 0;
     }
     __syncthreads();
-    // 2. warp 0 merges the sorted lists: lane l walks list l
-    if (warp == 0) {
-        int pos = 0;
-        unsigned long long head = lane < nw ? wl[lane * kMaxTopK] : 0ull;
-#pragma unroll 1
-        for (int j = 0; j < k; ++j) {
-            const unsigned long long best = warp_max_key(head);
-            if (head == best) {
-                ++pos;
-                head = pos < k ? wl[lane * kMaxTopK + pos] : 0ull;
-            }
-            if (lane == 0) {
-                const int e = 1023 - (int)(best & 1023ull);
+    // L: the k-th largest warp maximum (lanes past the warps hold zero)
+    unsigned long long thr;
+    {
+        unsigned long long m = lane < nw ? wmax[lane] : 0ull;
+        int r = 0;
+#pragma unroll 4
+        for (int x = 0; x < nw; ++x) r += wmax[x] > m ? 1 : 0;
+        // the lane whose maximum has exactly k - 1 larger ones holds L (maxima
+        // are distinct but for zeros; with fewer than k nonzero maxima L is 0)
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < nw && r == k - 1);
+        thr = hit ? __shfl_sync(0xffffffffu, m, __ffs(hit) - 1) : 0ull;
+    }
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(w.z64);
+    {
+        const bool in = key != 0ull && key >= thr;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&ncand, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (in && pos < kBlockCandMax) cand[pos] = key;
+    }
+    __syncthreads();
+    const int nc = ncand;
+    if (nc <= kBlockCandMax) {
+        if (tid < nc) {
+            const unsigned long long x = cand[tid];
+            int rank = 0;
+#pragma unroll 4
+            for (int u = 0; u < nc; ++u) rank += cand[u] > x ? 1 : 0;
+            if (rank < k) {
+                const int e = 1023 - (int)(x & 1023ull);
                 const float2 ze = w.z[e];
                 const float be = w.b[e];
-                w.sel[j] = e;
-                w.selz[j] = ze;
-                w.selb[j] = be;
-                lowb[j] = norm_pair(ze.x, __fsub_rd(ze.y, be));
+                w.sel[rank] = e;
+                w.selz[rank] = ze;
+                w.selb[rank] = be;
+                lowb[rank] = norm_pair(ze.x, __fsub_rd(ze.y, be));
+            }
+        }
+    } else {
+        // 1. each warp's k largest keys, in order (a popped key becomes zero)
+        {
+            unsigned long long mine = key;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                const unsigned long long best = warp_max_key(mine);
+                if (lane == 0) wl[warp * kMaxTopK + j] = best;
+                if (mine == best) mine = 0ull;
+            }
+        }
+        __syncthreads();
+        // 2. warp 0 merges the sorted lists: lane l walks list l
+        if (warp == 0) {
+            int pos = 0;
+            unsigned long long head = lane < nw ? wl[lane * kMaxTopK] : 0ull;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                const unsigned long long best = warp_max_key(head);
+                if (head == best) {
+                    ++pos;
+                    head = pos < k ? wl[lane * kMaxTopK + pos] : 0ull;
+                }
+                if (lane == 0) {
+                    const int e = 1023 - (int)(best & 1023ull);
+                    const float2 ze = w.z[e];
+                    const float be = w.b[e];
+                    w.sel[j] = e;
+                    w.selz[j] = ze;
+                    w.selb[j] = be;
+                    lowb[j] = norm_pair(ze.x, __fsub_rd(ze.y, be));
+                }
             }
         }
     }

@@ -323,6 +323,16 @@ def test_one_kernel_and_three_kernel_decode_agree_bitwise(fmt, pool_mode, E, T):
     one_vs_three_kernels(fmt, pool_mode, E, T, k, H=512, I=192, L=3, steps=6, has_shared=fmt in ("nvfp4", "q4_0"))
 
 
+@pytest.mark.parametrize("E,k", [(288, 12), (512, 16), (384, 16)])
+def test_one_token_wide_ranking_threshold_and_merge(E, k):
+    # One token over more than 256 experts: the persistent kernel ranks by a
+    # threshold selection, or by the sorted-list merge when the candidates
+    # overflow (288 experts fill 9 warps, fewer than k = 12 warp maxima, so
+    # every key is a candidate); both agree with the three-kernel path and the
+    # oracle.
+    one_vs_three_kernels("nvfp4", "shared", E, 1, k, H=512, I=192, L=2, steps=5, has_shared=True)
+
+
 @pytest.mark.parametrize("fmt,H,I,T,k,has_shared", [
     ("fp8_b128", 2048, 512, 8, 4, False),   # one ring slot
     ("q4_0", 2048, 512, 4, 8, False),       # three ring slots, refilled
