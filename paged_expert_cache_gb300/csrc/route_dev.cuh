@@ -964,7 +964,8 @@ __device__ __forceinline__ unsigned long long warp_min_key(unsigned long long ke
 // ascending order, into m.victims: the least recently used slots (keys are
 // the last-use stamps) or the LFU order (lfu_victim_keys). Keys are distinct,
 // except the ~0 of slots the call holds, which never rank among the nmiss
-// smallest. Thread t scans slots t, t + nthr, ... (at most 64 of them); each
+// smallest. A threshold selection (below) takes the usual case; otherwise
+// thread t scans slots t, t + nthr, ... (at most 64 of them); each
 // warp takes its nmiss smallest keys by nmiss rounds of a warp-wide minimum,
 // where the winning lane then looks for its next smallest, into m.vkey /
 // m.vslot; warp 0 merges the warps' sorted lists the same way. The same
@@ -972,6 +973,58 @@ __device__ __forceinline__ unsigned long long warp_min_key(unsigned long long ke
 // thread of the block calls it.
 __device__ __forceinline__ void select_victims(const PlanSmem& m, int K, int nmiss) {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    // Threshold selection first: U, the nmiss-th smallest of the warps'
+    // smallest keys, is at least the nmiss-th smallest key (nmiss warp minima
+    // are <= U), so the victims are among the keys <= U (a few for LRU
+    // stamps); each such candidate's rank is the number of candidates below it
+    // (keys are distinct). Small pools (under two keys per thread: the rounds
+    // are cheap there), too many candidates (ties at ~0) or more misses than
+    // warps: the rounds below.
+    if (K >= 2 * nthr) {
+        constexpr int kCandMax = 128;
+        __shared__ unsigned long long wmin[32];
+        __shared__ int ncand;
+        unsigned long long mn = ~0ull;
+        for (int i = tid; i < K; i += nthr) mn = min(mn, m.lu[i]);
+        const unsigned long long wm = warp_min_key(mn);
+        if (lane == 0) wmin[warp] = wm;
+        if (tid == 0) ncand = 0;
+        __syncthreads();
+        int nc = kCandMax + 1;
+        if (nmiss <= nw) {
+            const unsigned long long mine = lane < nw ? wmin[lane] : ~0ull;
+            int r = 0;
+            for (int x = 0; x < nw; ++x) r += wmin[x] < mine ? 1 : 0;
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < nw && r == nmiss - 1);
+            const unsigned long long u = hit ? __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1) : ~0ull;
+            for (int i0 = 0; i0 < K; i0 += nthr) {
+                const int i = i0 + tid;
+                const bool in = i < K && m.lu[i] <= u;
+                const unsigned bal = __ballot_sync(0xffffffffu, in);
+                int base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&ncand, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                if (in && pos < kCandMax) {
+                    m.vkey[pos] = m.lu[i];
+                    m.vslot[pos] = i;
+                }
+            }
+            __syncthreads();
+            nc = ncand;
+        }
+        if (nc <= kCandMax) {
+            if (tid < nc) {
+                const unsigned long long x = m.vkey[tid];
+                int rank = 0;
+                for (int y = 0; y < nc; ++y) rank += m.vkey[y] < x ? 1 : 0;
+                if (rank < nmiss) m.victims[rank] = m.vslot[tid];
+            }
+            __syncthreads();
+            return;
+        }
+        __syncthreads();  // the rounds below rewrite vkey / vslot
+    }
     unsigned long long taken = 0ull;  // bit r: slot tid + r * nthr is already a victim
     unsigned long long v = ~0ull;
     int sl = -1;
