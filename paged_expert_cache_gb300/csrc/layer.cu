@@ -753,13 +753,24 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     // to find its weights: unit j is pick j, read in place from its slot (the
     // descriptors the full plan gives such a call). The committing CTA still
     // runs the full plan, which also touches the slots and counts the hits.
-    __shared__ int fast;
+    // A single token with misses needs only the victims beyond that: unit j is
+    // still pick j; the hits are stamped in pick order as the full plan stamps
+    // them, and miss i in ascending expert order takes victim i (the full
+    // plan's first steps for one token, without its general dedupe and pair
+    // lists).
+    __shared__ int fast;  // 1: every pick resident; 2: one token with misses
     if (warp == 0) {
         int ok = 0;
         if (T == 1 && (!commit || defer)) {
             const int sl = lane < k ? m.smap[sids[lane]] : 0;
             ok = __all_sync(0xffffffffu, sl >= 0);
-            if (ok && lane <= k) {
+            if (!ok) {
+                const unsigned hb = __ballot_sync(0xffffffffu, lane < k && sl >= 0);
+                if (lane < k && sl >= 0) m.lu[sl] = clk + __popc(hb & ((1u << lane) - 1u));
+                const int nmiss = k - __popc(hb);
+                if (lane == 0) m.scal[1] = nmiss;
+                ok = nmiss <= kVictimLists && c.K <= 64 * kLThreads ? 2 : 0;
+            } else if (lane <= k) {
                 UnitDesc d;
                 d.pstart = 0;
                 d.np = 1;
@@ -787,7 +798,46 @@ __global__ void __launch_bounds__(kLThreads, 1) k_layer(const __grid_constant__ 
     }
     __syncthreads();
     int n_units;
-    if (fast) {
+    if (fast == 2) {
+        const int nmiss = m.scal[1];
+        if (c.lfu) lfu_victim_keys(c, m, clk);
+        select_victims(m, c.K, nmiss);
+        if (warp == 0 && lane <= k) {
+            UnitDesc d;
+            d.pstart = 0;
+            d.np = 1;
+#pragma unroll
+            for (int j = 1; j < 8; ++j) d.pair8[j] = -1;
+            d.pair8[0] = lane;
+            d.dst = 0;
+            d.hit = 1;
+            if (lane < k) {
+                const int e = sids[lane];
+                const int sl = m.smap[e];
+                d.expert = e;
+                for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[e * 3 + j] : 1.0f;
+                if (sl >= 0) {
+                    d.slot = sl;
+                    d.src = (uint64_t)(c.pool + ((size_t)pool * c.K + sl) * c.slot_stride);
+                } else {
+                    int r = 0;  // this miss's place among the misses, ascending expert
+                    for (int j = 0; j < k; ++j) r += (m.smap[sids[j]] < 0 && sids[j] < e) ? 1 : 0;
+                    const int v = m.victims[r];
+                    d.slot = v;
+                    d.hit = 0;
+                    d.src = (uint64_t)(c.store + ((size_t)a.layer * E + e) * c.slot_stride);
+                    d.dst = (uint64_t)(c.pool + ((size_t)pool * c.K + v) * c.slot_stride);
+                }
+            } else {
+                d.expert = -1;
+                d.slot = -1;
+                d.src = (uint64_t)(c.shared_w + (size_t)a.layer * c.slot_stride);
+                for (int j = 0; j < 3; ++j) d.g[j] = c.fmt == FMT_NVFP4 ? m.gl[E * 3 + j] : 1.0f;
+            }
+            if (lane < k || c.has_shared) sd[lane] = d;
+        }
+        n_units = k + (c.has_shared ? 1 : 0);
+    } else if (fast) {
         n_units = k + (c.has_shared ? 1 : 0);
     } else {
         plan_small(c, s, a, m, clk, sids, sd, commit && !defer);
