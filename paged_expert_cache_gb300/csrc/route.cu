@@ -68,6 +68,47 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(const __grid_constan
     plan_decode(c, s, a, m, clk, s.ids, s.units, true);
 }
 
+// Prefill logits: the prompt's tokens in tiles of kRoutePrefillTokens, the
+// CTA's kRouteWarps router rows staged in shared memory beside them (not held
+// in registers as the decode routing holds them), so two CTAs share an SM.
+// The same per-lane sums, butterfly and bounds as k_route's, so the same
+// logits; the token prescales come from the CTAs of the first expert column.
+constexpr int kRoutePrefillTokens = 16;
+
+__global__ void __launch_bounds__(kRouteThreads, 2) k_route_prefill(const __grid_constant__ CacheDev c,
+                                                                   const __grid_constant__ Scratch s,
+                                                                   const __grid_constant__ RouteArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait();
+    const int H = c.H, E = c.E, NT = kRoutePrefillTokens;
+    {
+        // the pairs' activation maxima start from zero for the expert kernels
+        const int P = a.T * c.k + (c.has_shared ? a.T : 0);
+        const int nthr = blockDim.x * gridDim.x * gridDim.y;
+        for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < P; i += nthr)
+            s.act_amax[i] = 0u;
+    }
+    const int t0 = blockIdx.y * NT, nt = min(NT, a.T - t0);
+    const int e0 = blockIdx.x * kRouteWarps, ne = min(kRouteWarps, E - e0);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);          // [NT][H]
+    uint16_t* wr = xs + (size_t)NT * H;                         // [kRouteWarps][H]
+    const int vpr = H / 8;
+    for (int i = threadIdx.x; i < nt * vpr; i += blockDim.x)
+        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(a.x + (size_t)t0 * H)[i];
+    for (int i = threadIdx.x; i < ne * vpr; i += blockDim.x)
+        reinterpret_cast<uint4*>(wr)[i] = __ldg(reinterpret_cast<const uint4*>(a.w + (size_t)e0 * H) + i);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0)
+        for (int tt = warp; tt < nt; tt += kRouteWarps) {
+            const unsigned m = token_absmax_warp(xs + (size_t)tt * H, H, lane);
+            if (lane == 0) s.tok_shift[t0 + tt] = token_shift(m);
+        }
+    if (warp >= ne) return;
+    router_logits_warp_smem<kRoutePrefillTokens>(c, a, xs, t0, nt, e0 + warp, wr + (size_t)warp * H, s.logits,
+                                                 s.bounds);
+}
+
 // Prefill: one warp per token.
 __global__ void __launch_bounds__(kRouteThreads) k_topk(const __grid_constant__ CacheDev c, const __grid_constant__ Scratch s,
                                                        const __grid_constant__ RouteArgs a) {
@@ -532,6 +573,17 @@ static void route_nt(const CacheDev& c, const Scratch& s, const RouteArgs& a, cu
 
 void launch_route(const CacheDev& c, const Scratch& s, const RouteArgs& a, int /*max_units*/, cudaStream_t st,
                   bool pdl) {
+    if (a.prefill) {
+        const size_t sm = (size_t)(kRoutePrefillTokens + kRouteWarps) * c.H * sizeof(uint16_t);
+        static size_t set = 0;
+        if (sm > set) {
+            cudaFuncSetAttribute(k_route_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            set = sm;
+        }
+        const dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (a.T + kRoutePrefillTokens - 1) / kRoutePrefillTokens);
+        launch_ex(k_route_prefill, grid, dim3(kRouteThreads), sm, st, pdl, c, s, a);
+        return;
+    }
     if (a.T <= 1) route_nt<1>(c, s, a, st, pdl);
     else if (a.T <= 2) route_nt<2>(c, s, a, st, pdl);
     else if (a.T <= 4) route_nt<4>(c, s, a, st, pdl);

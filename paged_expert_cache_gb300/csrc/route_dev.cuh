@@ -108,12 +108,13 @@ __device__ __forceinline__ void router_row_load(const uint16_t* w, int e, int H,
 __device__ __forceinline__ float router_chain(int H) { return (float)(8 * router_nvec(H) + 16); }
 
 // Logits of expert e for tokens t0 .. t0+nt-1 (staged bf16 in xs, [NT][H]),
-// one warp, with their bounds. Each lane sums its own columns in order with
+// one warp, with their bounds; row_vec(i, cb) gives the lane's i-th router
+// vector (columns cb .. cb + 7). Each lane sums its own columns in order with
 // an error-free two-sum, then the lanes combine in a fixed butterfly, so the
 // pair does not depend on which CTA or warp computes it.
-template <int NT>
-static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a, const uint16_t* xs, int t0, int nt, int e,
-                                   const uint4 (&wv)[kRouterMaxVec], float2* logits, float* bounds) {
+template <int NT, class RowVec>
+static __device__ void router_logits_warp_f(const CacheDev& c, const RouteArgs& a, const uint16_t* xs, int t0, int nt,
+                                            int e, RowVec&& row_vec, float2* logits, float* bounds) {
     const int H = c.H, E = c.E, lane = threadIdx.x & 31;
     float hi[NT], lo[NT], ab[NT];
 #pragma unroll
@@ -124,8 +125,9 @@ static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a,
         if (i >= nvec) break;
         const int cb = lane * 8 + i * 256;
         if (cb >= H) continue;  // the partial last round
-        float wf[8] = {bf16_lo(wv[i].x), bf16_hi(wv[i].x), bf16_lo(wv[i].y), bf16_hi(wv[i].y),
-                       bf16_lo(wv[i].z), bf16_hi(wv[i].z), bf16_lo(wv[i].w), bf16_hi(wv[i].w)};
+        const uint4 wvi = row_vec(i, cb);
+        float wf[8] = {bf16_lo(wvi.x), bf16_hi(wvi.x), bf16_lo(wvi.y), bf16_hi(wvi.y),
+                       bf16_lo(wvi.z), bf16_hi(wvi.z), bf16_lo(wvi.w), bf16_hi(wvi.w)};
 #pragma unroll
         for (int tt = 0; tt < NT; ++tt) {
             if (NT == 1 || tt < nt) {
@@ -184,6 +186,24 @@ static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a,
         logits[(size_t)(t0 + lane) * E + e] = z;
         bounds[(size_t)(t0 + lane) * E + e] = beta;
     }
+}
+
+// Logits of expert e for tokens t0 .. t0+nt-1 (staged bf16 in xs, [NT][H]),
+// one warp, with their bounds: the lane's router vectors held in registers
+// (wv, loaded by router_row_load) ...
+template <int NT>
+static __device__ void router_logits_warp(const CacheDev& c, const RouteArgs& a, const uint16_t* xs, int t0, int nt, int e,
+                                          const uint4 (&wv)[kRouterMaxVec], float2* logits, float* bounds) {
+    router_logits_warp_f<NT>(c, a, xs, t0, nt, e, [&](int i, int) { return wv[i]; }, logits, bounds);
+}
+
+// ... or read from the router row staged in shared memory (row: its first
+// element): the same vectors, sums and bounds.
+template <int NT>
+static __device__ void router_logits_warp_smem(const CacheDev& c, const RouteArgs& a, const uint16_t* xs, int t0, int nt,
+                                               int e, const uint16_t* row, float2* logits, float* bounds) {
+    router_logits_warp_f<NT>(
+        c, a, xs, t0, nt, e, [&](int, int cb) { return *reinterpret_cast<const uint4*>(row + cb); }, logits, bounds);
 }
 
 // The same logit and bound for one token, with the router row staged in
