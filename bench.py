@@ -578,7 +578,8 @@ def run_ours(args):
     gbs = lambda nbytes, us: nbytes / (us * 1e-6) / 1e9 if us else None
     gu_gbs = gbs(gu_bytes, gu_hit)
     dn_gbs = gbs(dn_bytes, dn_hit)
-    fused = ly_hit is not None
+    # the path the calls took (not whether an all-hit call happened to be profiled)
+    fused = any(p["layer"]["launches"] for _, p in calls)
     # one call's algorithmic bytes: router, tokens, every unit's record once,
     # activations written and read back, the output
     call_bytes = rt_bytes + units * rec_bytes + 2 * units * T * w.I * 4 + T * w.H * 4
@@ -609,7 +610,7 @@ def run_ours(args):
     if os.path.exists(tfile):
         try:
             tj = json.load(open(tfile))
-            if tj.get("workload") == w.name and tj.get("kernel") == ("layer" if ly_hit is not None else "gateup"):
+            if tj.get("workload") == w.name and tj.get("kernel") == ("layer" if fused else "gateup"):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
